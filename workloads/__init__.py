@@ -1,0 +1,175 @@
+"""Seeded synthetic inputs for frame-aligned sparse attention.
+
+This module only draws random tensors and rounds them to bf16.  It holds none
+of the attention arithmetic: no mask, no softmax, no bound.  Both the fp64
+oracle (``oracle/``) and the CUDA path's tests and benchmark take their inputs
+from here, so the two sides see the same bits.
+
+Shapes follow the super-resolution workloads described in "HeyGen x Google
+Cloud: Avatar IV on TPU" (news.xcc.im/article/5328), sections "The Workload,
+and the Port" (720p / 1080p output, 25 fps) and "Deleting the Mask" (tens of
+thousands of tokens per chunk, one reference frame plus a window of frames,
+frame spans that are not multiples of 128).
+
+Token order is frame-contiguous: the reference frame(s) first, then the video
+frames in time order, ``frame_tokens`` tokens each.  Tensors are ``[H, N, d]``
+with ``N = (ref_frames + n_frames) * frame_tokens``.
+
+Recipe (every draw has its own counter-free stream, so any head can be made
+alone and in any order):
+
+* stream ``(seed, 0, h)``: ``q[h] ~ N(0, 1)`` as float32 ``[N, d]``
+* stream ``(seed, 1, h)``: key noise ``~ N(0, 1)`` float32 ``[N, d]``
+* stream ``(seed, 2, h)``: ``v[h] ~ N(0, 1)`` float32 ``[N, d]``
+* stream ``(seed, 3, h)``: the common key vector ``mu_h ~ N(0, 1)`` (float64,
+  ``[d]``); ``k[h] = noise + float32(sigma * mu_h)``
+* stream ``(seed, 4)``: ``permutation(H)``; its first ``n_modified`` entries
+  are the modified heads
+* ``"qscale"`` modifier: ``q[h] *= 8`` on the modified heads (loose bound)
+* ``"heavy"`` modifier: on the modified heads the key noise is instead drawn
+  from stream ``(seed, 5, h)`` as Student-t with 3 degrees of freedom, and
+  ``N // 100`` rows chosen by stream ``(seed, 6, h)`` (without replacement)
+  have that noise multiplied by 4 (norm outliers)
+* every tensor is rounded once from float32 to bf16, round-to-nearest-even.
+
+Arrays are returned as raw bf16 bit patterns (``numpy.uint16``).
+"""
+from __future__ import annotations
+
+import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
+from typing import Dict, Iterable, Optional, Sequence
+
+import numpy as np
+
+__all__ = ["Workload", "WORKLOADS", "get", "generate", "round_to_bf16_bits"]
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    heads: int          # H (batch folded in; B = 1 everywhere)
+    head_dim: int       # d
+    ref_frames: int     # R0
+    n_frames: int       # F (video frames)
+    frame_tokens: int   # T
+    window_radius: int  # r
+    sigma: float        # scale of the common key vector
+    seed: int
+    modifier: Optional[str] = None  # None | "qscale" | "heavy"
+    n_modified: int = 0
+
+    @property
+    def total_frames(self) -> int:
+        return self.ref_frames + self.n_frames
+
+    @property
+    def tokens(self) -> int:
+        return self.total_frames * self.frame_tokens
+
+    def describe(self) -> str:
+        return (f"{self.name}: H={self.heads} d={self.head_dim} "
+                f"{self.ref_frames} ref + {self.n_frames} frames x "
+                f"{self.frame_tokens} tokens (N={self.tokens}), "
+                f"window radius {self.window_radius}, sigma={self.sigma}, "
+                f"seed={self.seed}, modifier={self.modifier}"
+                f"{'x' + str(self.n_modified) if self.modifier else ''}")
+
+
+WORKLOADS: Dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("tiny", 2, 64, 1, 8, 48, 1, 2.0, 0),
+        Workload("mid", 16, 128, 1, 16, 880, 2, 3.0, 1),
+        Workload("720p", 24, 128, 1, 21, 3600, 2, 3.0, 2, "qscale", 2),
+        Workload("1080p", 24, 128, 1, 13, 8160, 1, 3.0, 3),
+        Workload("stress", 24, 128, 1, 21, 3600, 2, 3.0, 4, "heavy", 12),
+        # Same tensors as "stress" (same seed and modifier); every frame visible.
+        Workload("dense", 24, 128, 1, 21, 3600, 21, 3.0, 4, "heavy", 12),
+    ]
+}
+
+
+def get(name: str) -> Workload:
+    return WORKLOADS[name]
+
+
+def _stream(*key: int) -> np.random.Generator:
+    return np.random.default_rng(np.random.SeedSequence(list(key)))
+
+
+def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns, round to nearest, ties to even.
+
+    Inputs here are finite and far from the float32 range limits.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def modified_heads(w: Workload) -> np.ndarray:
+    """Sorted indices of the heads that the workload's modifier touches."""
+    if not w.modifier:
+        return np.zeros(0, dtype=np.int64)
+    perm = _stream(w.seed, 4).permutation(w.heads)
+    return np.sort(perm[: w.n_modified])
+
+
+def _make_head(w: Workload, tensor: str, h: int, modified: bool) -> np.ndarray:
+    n, d = w.tokens, w.head_dim
+    if tensor == "q":
+        x = _stream(w.seed, 0, h).standard_normal((n, d), dtype=np.float32)
+        if modified and w.modifier == "qscale":
+            x *= np.float32(8.0)
+    elif tensor == "k":
+        if modified and w.modifier == "heavy":
+            x = _stream(w.seed, 5, h).standard_t(3, (n, d)).astype(np.float32)
+            rows = _stream(w.seed, 6, h).choice(n, n // 100, replace=False)
+            x[rows] *= np.float32(4.0)
+        else:
+            x = _stream(w.seed, 1, h).standard_normal((n, d), dtype=np.float32)
+        mu = _stream(w.seed, 3, h).standard_normal(d)
+        x += (w.sigma * mu).astype(np.float32)[None, :]
+    elif tensor == "v":
+        x = _stream(w.seed, 2, h).standard_normal((n, d), dtype=np.float32)
+    else:
+        raise ValueError(tensor)
+    return round_to_bf16_bits(x)
+
+
+def generate(w: Workload | str,
+             tensors: Sequence[str] = ("q", "k", "v"),
+             heads: Optional[Iterable[int]] = None,
+             workers: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Draw the workload's tensors as bf16 bits, ``[len(heads), N, d]`` each.
+
+    ``heads`` defaults to all heads.  The result also carries
+    ``"modified_heads"`` (indices into the full head range).
+    """
+    if isinstance(w, str):
+        w = get(w)
+    hs = list(range(w.heads)) if heads is None else [int(h) for h in heads]
+    mod = set(modified_heads(w).tolist())
+    out: Dict[str, np.ndarray] = {}
+    jobs = []
+    for t in tensors:
+        arr = np.empty((len(hs), w.tokens, w.head_dim), dtype=np.uint16)
+        out[t] = arr
+        for i, h in enumerate(hs):
+            jobs.append((arr, i, t, h))
+
+    def run(job):
+        arr, i, t, h = job
+        arr[i] = _make_head(w, t, h, h in mod)
+
+    nw = workers or min(len(jobs), os.cpu_count() or 1, 16)
+    if nw <= 1 or len(jobs) <= 1:
+        for j in jobs:
+            run(j)
+    else:
+        with ThreadPoolExecutor(max_workers=nw) as ex:
+            list(ex.map(run, jobs))
+    out["modified_heads"] = modified_heads(w)
+    return out
