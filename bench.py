@@ -1,0 +1,398 @@
+"""Benchmark: frame-aligned sparse attention on GB300.
+
+One step = one pass of the whole hot path over one synthetic 720p-like SR
+chunk (1 reference + 21 frames x 3600 tokens, 24 heads, d=128, window radius
+2): the key/query prepass (mean-centred norms, row bounds, eligibility) and
+the single-pass attention kernel.  The plan (block table, work list) is built
+once per shape; fas_plan is still called every step and returns at once.
+
+value = visible-block FLOPs (4*d per visible (query, key) pair, valid rows
+only) of all ranks / time of the timed steps.  Inputs (1.46 GB of Q/K/V) are
+larger than L2, so no flush is needed between steps.
+
+Arms:
+  python bench.py [--gpus N] [--steps K] [--warmup W]     this library
+  python bench.py --impl reference ...                      the fp64 oracle on
+      the host cores, a bounded sample of the same workload per step
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "visible-block attention TFLOP/s & % GB300 BF16 peak; ms per 720p SR chunk"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def visible_flops(w) -> float:
+    """4*d per visible pair, from the frame rule (reference global both ways,
+    window clipped to the video frames)."""
+    nf = w.total_frames
+    frames = 0
+    for f in range(nf):
+        if f < w.ref_frames:
+            frames += nf
+        else:
+            lo, hi = max(w.ref_frames, f - w.window_radius), min(nf - 1, f + w.window_radius)
+            frames += w.ref_frames + hi - lo + 1
+    return 4.0 * w.head_dim * w.heads * frames * w.frame_tokens ** 2
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_fingerprint() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "frame_aligned_sparse_gb300", "csrc")
+    for name in ("attention.cu", "ptx.cuh", "kernels.h", "internal.h"):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "attention_fwd_720p.md")
+    if not os.path.exists(path):
+        return None
+    fp = kernel_fingerprint()
+    for line in open(path):
+        if line.startswith("traffic_per_launch_bytes:"):
+            parts = line.split()
+            if len(parts) >= 4 and parts[3] == fp:
+                return float(parts[1])
+    return None
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(w, x, units, budget_s=None):
+    """Runs the oracle on whole query tiles (128 rows of one frame) of head
+    h, in the given order, until the list or the time budget ends.  Returns
+    (visible FLOPs done, seconds, tiles done)."""
+    import oracle
+    T, nf = w.frame_tokens, w.total_frames
+    flops = 0.0
+    t0 = time.perf_counter()
+    done = 0
+    for h, f, t in units:
+        rows = np.arange(f * T + t * 128, f * T + min(T, (t + 1) * 128))
+        oracle.masked_attention(x["q"], x["k"], x["v"], T, w.ref_frames, w.window_radius, rows=rows, heads=[h])
+        vis = len(oracle.visible_frames(f, nf, w.ref_frames, w.window_radius)) * T
+        flops += 4.0 * w.head_dim * len(rows) * vis
+        done += 1
+        if budget_s is not None and time.perf_counter() - t0 >= budget_s:
+            break
+    return flops, time.perf_counter() - t0, done
+
+
+def tile_order(w, seed=0):
+    tiles = -(-w.frame_tokens // 128)
+    units = [(h, f, t) for h in range(w.heads) for f in range(w.total_frames) for t in range(tiles)]
+    rng = np.random.default_rng(seed)
+    return [units[i] for i in rng.permutation(len(units))]
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    x = workloads.generate(w)
+    order = tile_order(w)
+    per_step = 4  # query tiles (512 rows) per step
+    pos = 0
+
+    def step():
+        nonlocal pos
+        units = [order[(pos + i) % len(order)] for i in range(per_step)]
+        pos += per_step
+        return oracle_sample(w, x, units)
+
+    for _ in range(args.warmup):
+        step()
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f_, s_, _ = step()
+        flops += f_
+        secs += s_
+    value = flops / secs / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.describe(), "sample_per_step": f"{per_step} query tiles of 128 rows"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} random query tiles (128 rows, one head) per step, fp64 dense "
+                                   f"masked attention over all {w.tokens} keys"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# The library arm
+# ----------------------------------------------------------------------------
+
+def run_fas(args, w):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from frame_aligned_sparse_gb300 import build as fas_build
+    fas_build.build()
+    import frame_aligned_sparse_gb300 as fas
+
+    x = workloads.generate(w)
+    host = {t: torch.from_numpy(x[t].view(np.int16)).view(torch.bfloat16) for t in "qkv"}
+    q, k, v = (host[t].to(dev) for t in "qkv")
+    H, N, d = w.heads, w.tokens, w.head_dim
+    out = torch.empty_like(q)
+    lse = torch.empty(H, N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = visible_flops(w)
+
+    def plan():
+        return fas.fas_plan(w.frame_tokens, w.n_frames, w.ref_frames, w.window_radius, H, d, block_k=args.block_k)
+
+    info = plan()
+    assert abs(info.visible_flops - flops) < 1.0
+
+    launches = [0]
+
+    def step(ev=None):
+        plan()
+        fas.fas_prepass(q, k, stream=stream)
+        launches[0] += fas.fas_last_launch_count()
+        if ev is not None:
+            ev[0].record(stream)
+        fas.fas_forward(q, k, v, out, lse, mode=args.mode, stream=stream)
+        launches[0] += fas.fas_last_launch_count()
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    if fas.fas_status(stream) != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+    elig = fas.fas_prepass(q, k, stream=stream, want_elig=True)
+
+    sampler = ClockSampler(local)
+    fwd_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.2)
+    launches[0] = 0
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(fwd_events[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    if fas.fas_status(stream) != 0:
+        raise RuntimeError("device-side wait timed out in the timed region")
+    ms_total = t_start.elapsed_time(t_end)
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_events]
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    prepass_ms = ms_step - fwd_avg
+
+    # End to end through the public API: pinned host inputs in, host results out.
+    pin = {t: host[t].pin_memory() for t in "qkv"}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for t, dst in (("q", q), ("k", k), ("v", v)):
+            dst.copy_(pin[t], non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = sum(pin[t].numel() * 2 for t in "qkv")
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (fwd_avg * 1e-3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f_, s_, n_ = oracle_sample(w, x, tile_order(w, seed=1), budget_s=args.cpu_budget)
+        cpu = {"value": f_ / s_ / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n_} random query tiles (128 rows, one head each) of the {w.name} workload, "
+                         f"fp64 dense masked attention over all {w.tokens} keys, {s_:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, 720p-like SR chunk)",
+        "config": {
+            "workload": w.describe(), "mode": args.mode, "block_k": info.block_k, "q_tile": info.q_tile,
+            "work_items": info.n_work, "visible_tflop_per_step": flops / 1e12,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs (1.46 GB Q/K/V) larger than L2; no flush",
+            "eligible_heads": int(elig.sum()),
+        },
+        "ms_per_chunk": fwd_avg,
+        "pct_bf16_peak": 100.0 * achieved / peak,
+        "prepass": {"ms": prepass_ms, "gbs": 3 * H * N * d * 2 / (prepass_ms * 1e-3) / 1e9,
+                    "bytes": "K read twice + Q read once"},
+        "roofline": {"bound": "tensor", "kernel": "attention_fwd", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"bf16_tflops ({peak_src})",
+                     "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                     "traffic": recorded_traffic()},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches[0],
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    fas.fas_free()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["fas", "reference"], default="fas")
+    ap.add_argument("--workload", default="720p", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--mode", default="auto", choices=["auto", "online", "bounded"])
+    ap.add_argument("--block-k", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    w = workloads.get(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_fas(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,237 @@
+"""Frame-aligned sparse attention for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over the C ABI in ``include/fas.h`` (``libfas.so``).  It
+only marshals arguments: every step of the computation runs in the library's
+CUDA kernels.  PyTorch supplies device memory and streams.  If the library is
+not built, every call raises: there is no CPU fallback.
+
+The operation ("HeyGen x Google Cloud: Avatar IV on TPU", sections "Deleting
+the Mask" and "Unchaining the Softmax"): queries of each video frame attend
+to a window of neighbouring frames plus the global reference frame(s), in one
+pass over frame-aligned full key blocks; eligible heads use a precomputed
+Cauchy-Schwarz row bound instead of a running maximum.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+
+__all__ = [
+    "FasError", "PlanInfo", "MODES", "library_path", "load",
+    "fas_plan", "fas_plan_describe", "fas_prepass", "fas_forward", "fas_free",
+    "fas_status", "fas_prepass_readback", "fas_selftest_wait_timeout", "fas_last_launch_count",
+]
+
+FAS_OK, FAS_ERR_ARG, FAS_ERR_STATE, FAS_ERR_ALIGN, FAS_ERR_CUDA, FAS_ERR_TIMEOUT, FAS_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+MODES = {"auto": 0, "online": 1, "bounded": 2}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libfas.so")
+
+
+class FasError(RuntimeError):
+    def __init__(self, call: str, code: int, message: str):
+        super().__init__(f"{call} failed: {message} (status {code})")
+        self.code = code
+
+
+class _PlanInfoC(ctypes.Structure):
+    _fields_ = [
+        ("block_k", ctypes.c_int32),
+        ("q_tile", ctypes.c_int32),
+        ("n_work", ctypes.c_int32),
+        ("total_frames", ctypes.c_int32),
+        ("tokens", ctypes.c_int64),
+        ("key_blocks", ctypes.c_int64),
+        ("visible_flops", ctypes.c_double),
+        ("host_table", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
+@dataclasses.dataclass
+class PlanInfo:
+    block_k: int
+    q_tile: int
+    n_work: int
+    total_frames: int
+    tokens: int
+    key_blocks: int
+    visible_flops: float
+    table: np.ndarray  # [Nf, 4] int32: start0, len0, start1, len1
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+_SIGS = {
+    "fas_plan": (ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.POINTER(_PlanInfoC)]),
+    "fas_plan_ex": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(_PlanInfoC)]),
+    "fas_plan_describe": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(_PlanInfoC), ctypes.c_void_p,
+                                                              ctypes.c_void_p]),
+    "fas_prepass": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "fas_forward": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_void_p]),
+    "fas_free": (ctypes.c_int, []),
+    "fas_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "fas_prepass_readback": (ctypes.c_int, [ctypes.c_void_p] * 6),
+    "fas_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p]),
+    "fas_last_launch_count": (ctypes.c_int, []),
+    "fas_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def load() -> ctypes.CDLL:
+    """Loads libfas.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m frame_aligned_sparse_gb300.build` "
+                "(nvcc, sm_103a). There is no CPU fallback.")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(call: str, rc: int) -> None:
+    if rc != FAS_OK:
+        msg = load().fas_error_string(rc).decode()
+        raise FasError(call, rc, msg)
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _info(c: _PlanInfoC, table: Optional[np.ndarray] = None) -> PlanInfo:
+    if table is None:
+        table = np.ctypeslib.as_array(c.host_table, shape=(c.total_frames * 4,)).reshape(-1, 4).copy()
+    return PlanInfo(c.block_k, c.q_tile, c.n_work, c.total_frames, c.tokens, c.key_blocks, c.visible_flops, table)
+
+
+_PLAN: dict = {}
+
+
+def fas_plan(frame_tokens: int, n_frames: int, ref_frames: int, window_radius: int, heads: int, head_dim: int,
+             block_k: int = 0) -> PlanInfo:
+    """Builds (or reuses) the library's plan; see ``fas_plan`` in fas.h."""
+    c = _PlanInfoC()
+    rc = load().fas_plan_ex(frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k,
+                            ctypes.byref(c))
+    _check("fas_plan", rc)
+    info = _info(c)
+    _PLAN.update(heads=heads, head_dim=head_dim, tokens=info.tokens, info=info)
+    return info
+
+
+def fas_plan_describe(frame_tokens: int, n_frames: int, ref_frames: int, window_radius: int, heads: int,
+                      head_dim: int, block_k: int = 0) -> Tuple[PlanInfo, np.ndarray, np.ndarray]:
+    """Host-only plan: (info, table [Nf, 4], work [n_work, 4])."""
+    lib = load()
+    c = _PlanInfoC()
+    _check("fas_plan_describe", lib.fas_plan_describe(frame_tokens, n_frames, ref_frames, window_radius, heads,
+                                                      head_dim, block_k, ctypes.byref(c), None, None))
+    table = np.zeros((c.total_frames, 4), dtype=np.int32)
+    work = np.zeros((c.n_work, 4), dtype=np.int32)
+    _check("fas_plan_describe", lib.fas_plan_describe(frame_tokens, n_frames, ref_frames, window_radius, heads,
+                                                      head_dim, block_k, ctypes.byref(c),
+                                                      table.ctypes.data, work.ctypes.data))
+    return _info(c, table), table, work
+
+
+def _check_tensor(name, t, shape, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, the plan needs {tuple(shape)}")
+
+
+def _qkv_shape():
+    if not _PLAN:
+        raise FasError("fas_plan", FAS_ERR_STATE, "no plan")
+    return (_PLAN["heads"], _PLAN["tokens"], _PLAN["head_dim"])
+
+
+def fas_prepass(q, k, stream=None, want_elig: bool = False) -> Optional[np.ndarray]:
+    """Mean-centred key norms, row bounds and head eligibility (bf16 q, k [H, N, d])."""
+    import torch
+    shape = _qkv_shape()
+    _check_tensor("q", q, shape, torch.bfloat16)
+    _check_tensor("k", k, shape, torch.bfloat16)
+    elig = np.zeros(shape[0], dtype=np.uint8) if want_elig else None
+    rc = load().fas_prepass(q.data_ptr(), k.data_ptr(), _stream_handle(stream),
+                            elig.ctypes.data if want_elig else None)
+    _check("fas_prepass", rc)
+    return elig
+
+
+def fas_forward(q, k, v, out=None, lse=None, mode: str = "auto", stream=None):
+    """Attention; returns (out bf16 [H, N, d], lse fp32 [H, N])."""
+    import torch
+    shape = _qkv_shape()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(name, t, shape, torch.bfloat16)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(shape[:2], dtype=torch.float32, device=q.device)
+    _check_tensor("out", out, shape, torch.bfloat16)
+    _check_tensor("lse", lse, shape[:2], torch.float32)
+    rc = load().fas_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                            MODES[mode], _stream_handle(stream))
+    _check("fas_forward", rc)
+    return out, lse
+
+
+def fas_free() -> None:
+    _PLAN.clear()
+    _check("fas_free", load().fas_free())
+
+
+def fas_status(stream=None) -> int:
+    """Synchronises the stream; returns FAS_OK or FAS_ERR_TIMEOUT (raises on other errors)."""
+    rc = load().fas_status(_stream_handle(stream))
+    if rc not in (FAS_OK, FAS_ERR_TIMEOUT):
+        _check("fas_status", rc)
+    return rc
+
+
+def fas_prepass_readback(stream=None, row_bound: bool = False) -> dict:
+    H, N, d = _qkv_shape()
+    nf = _PLAN["info"].total_frames
+    res = {"mu": np.zeros((H, d), np.float32), "frame_max": np.zeros((H, nf), np.float32),
+           "stat": np.zeros(H, np.float32), "elig": np.zeros(H, np.uint8)}
+    rb = np.zeros((H, N), np.float32) if row_bound else None
+    rc = load().fas_prepass_readback(res["mu"].ctypes.data, res["frame_max"].ctypes.data, res["stat"].ctypes.data,
+                                     res["elig"].ctypes.data, rb.ctypes.data if row_bound else None,
+                                     _stream_handle(stream))
+    _check("fas_prepass_readback", rc)
+    if row_bound:
+        res["row_bound"] = rb
+    return res
+
+
+def fas_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    return load().fas_selftest_wait_timeout(limit_us, _stream_handle(stream))
+
+
+def fas_last_launch_count() -> int:
+    return load().fas_last_launch_count()

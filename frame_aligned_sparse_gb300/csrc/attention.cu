@@ -1,0 +1,429 @@
+// Frame-aligned sparse attention, single pass, for sm_103a.
+//
+// "HeyGen x Google Cloud: Avatar IV on TPU":
+//  - "Deleting the Mask" (Fig. 3): key blocks divide the frame's token span,
+//    so every visible block is full; the kernel walks the (at most two)
+//    visible key ranges of its query frame block by block — the reference
+//    frame's blocks are just more blocks of the same softmax.  No mask
+//    predicate, no padding, no second pass, no merge.
+//  - "Unchaining the Softmax" (Fig. 4): eligible heads use a fixed per-row
+//    maximum m_i (precomputed Cauchy-Schwarz bound), so the inner loop has no
+//    running max and no rescale; other heads run the online softmax (running
+//    max, conditional rescale of the accumulator) inside the same kernel.
+//  - "Proving the Pixels Didn't Change": the P.V product runs in bf16 on the
+//    tensor cores with fp32 accumulation.
+//
+// One CTA per work item (head h, query frame f, query tile of 128 rows).
+//   warps 0-3  softmax + epilogue; thread t owns row t of the tile, which is
+//              TMEM lane t (warp w reads lanes 32w..32w+31)
+//   warp 4     TMA producer: Q tile once, then K and V blocks into rings
+//   warp 5     TMEM allocator and tcgen05.mma issuer (one thread)
+// TMEM (512 columns): O at [0, d), S buffers at 128 and 128 + roundup32(Bk).
+// P (bf16) overwrites the first Bk/2 columns of its S buffer and feeds the
+// P.V MMA straight from TMEM.
+// MMA issue order: S0, S1, PV0, S2, PV1, ...; the tensor pipe executes them
+// in order, so S(j+2) never overwrites P(j) before PV(j) has read it.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fas.h"
+#include "internal.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fas {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;
+constexpr uint32_t kColS0 = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// Online path: keep the current maximum until a block raises it by more than
+// 2^8; probabilities then stay below 256 (safe in fp32 and bf16).
+constexpr float kRescaleThreshold = 8.0f;
+
+struct Barriers {
+  uint64_t q_full;
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done;
+  uint64_t o_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint32_t s_col(int buf, int Bk) {
+  return buf == 0 ? kColS0 : kColS0 + ((uint32_t)(Bk + 31) & ~31u);
+}
+
+// Wait with no abort check (used only to drain in-flight copies and MMAs).
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsigned int* err, uint64_t limit) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::global_timer_ns() - t0 > limit) {
+      atomicOr(err, kErrWaitDrain);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int D>
+__device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                         Barriers& bars, uint32_t q_s, uint32_t k_s0, uint32_t v_s0, int h, int f,
+                                         int qt, int4 rng, const FwdParams& p) {
+  volatile int* abort_flag = &bars.abort;
+  const uint32_t kv_bytes = (uint32_t)p.Bk * D * 2;
+  const uint32_t half_bytes = (uint32_t)p.Bk * 128;
+  ptx::mbar_arrive_expect_tx(ptx::smem_addr(&bars.q_full), kQTile * D * 2);
+#pragma unroll
+  for (int half = 0; half < D / 64; ++half)
+    ptx::tma_load_4d(q_s + half * (kQTile * 128), tm_q, ptx::smem_addr(&bars.q_full), half * 64, qt * kQTile, f, h);
+
+  int k_fills[kKStages] = {0, 0};
+  int v_fills[kVStages] = {0, 0};
+  bool ok = true;
+  int j = 0;
+  for (int part = 0; part < 2 && ok; ++part) {
+    const int start = part == 0 ? rng.x : rng.z;
+    const int len = part == 0 ? rng.y : rng.w;
+    for (int key = start; key < start + len; key += p.Bk, ++j) {
+      const int ks = j % kKStages, uk = j / kKStages;
+      if (uk >= 1 &&
+          !ptx::mbar_wait(ptx::smem_addr(&bars.k_empty[ks]), (uk - 1) & 1, abort_flag, p.err, kErrWaitProducer,
+                          p.limit_ns)) {
+        ok = false;
+        break;
+      }
+      const uint32_t kfull = ptx::smem_addr(&bars.k_full[ks]);
+      ptx::mbar_arrive_expect_tx(kfull, kv_bytes);
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half)
+        ptx::tma_load_3d(k_s0 + ks * kv_bytes + half * half_bytes, tm_k, kfull, half * 64, key, h);
+      ++k_fills[ks];
+
+      const int vs = j % kVStages, uv = j / kVStages;
+      if (uv >= 1 &&
+          !ptx::mbar_wait(ptx::smem_addr(&bars.v_empty[vs]), (uv - 1) & 1, abort_flag, p.err, kErrWaitProducer,
+                          p.limit_ns)) {
+        ok = false;
+        break;
+      }
+      const uint32_t vfull = ptx::smem_addr(&bars.v_full[vs]);
+      ptx::mbar_arrive_expect_tx(vfull, kv_bytes);
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half)
+        ptx::tma_load_3d(v_s0 + vs * kv_bytes + half * half_bytes, tm_v, vfull, half * 64, key, h);
+      ++v_fills[vs];
+    }
+  }
+  if (!ok) {
+    // Let every copy this thread started land before the CTA exits.
+    drain_wait(ptx::smem_addr(&bars.q_full), 0, p.err, p.limit_ns);
+    for (int s = 0; s < kKStages; ++s)
+      if (k_fills[s] > 0) drain_wait(ptx::smem_addr(&bars.k_full[s]), (k_fills[s] - 1) & 1, p.err, p.limit_ns);
+    for (int s = 0; s < kVStages; ++s)
+      if (v_fills[s] > 0) drain_wait(ptx::smem_addr(&bars.v_full[s]), (v_fills[s] - 1) & 1, p.err, p.limit_ns);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32_t q_s, uint32_t k_s0,
+                                           uint32_t v_s0, int nblk, const FwdParams& p) {
+  volatile int* abort_flag = &bars.abort;
+  const uint32_t kv_bytes = (uint32_t)p.Bk * D * 2;
+  const uint32_t half_bytes = (uint32_t)p.Bk * 128;
+  const uint32_t idesc_s = ptx::idesc_bf16_f32(kQTile, (uint32_t)p.Bk, false);
+  const uint32_t idesc_o = ptx::idesc_bf16_f32(kQTile, D, true);
+  bool ok = ptx::mbar_wait(ptx::smem_addr(&bars.q_full), 0, abort_flag, p.err, kErrWaitMma, p.limit_ns);
+  for (int j = 0; ok && j <= nblk; ++j) {
+    if (j < nblk) {
+      // S(j) = Q . K(j)^T : M=128, N=Bk, K=d; both operands K-major, 128B swizzle.
+      const int ks = j % kKStages;
+      if (!ptx::mbar_wait(ptx::smem_addr(&bars.k_full[ks]), (j / kKStages) & 1, abort_flag, p.err, kErrWaitMma,
+                          p.limit_ns)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after_sync();
+      const uint32_t kb = k_s0 + ks * kv_bytes;
+      const uint32_t d_s = tmem + s_col(j & 1, p.Bk);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t a = q_s + (kk >> 2) * (kQTile * 128) + (kk & 3) * 32;
+        const uint32_t b = kb + (kk >> 2) * half_bytes + (kk & 3) * 32;
+        ptx::mma_ss(d_s, ptx::smem_desc_sw128(a, 16, 1024), ptx::smem_desc_sw128(b, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(ptx::smem_addr(&bars.s_full[j & 1]));
+      ptx::mma_commit(ptx::smem_addr(&bars.k_empty[ks]));
+    }
+    if (j >= 1) {
+      // O += P(i) . V(i) : M=128, N=d, K=Bk; P from TMEM, V MN-major in smem.
+      const int i = j - 1;
+      const int vs = i % kVStages;
+      if (!ptx::mbar_wait(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err, kErrWaitMma,
+                          p.limit_ns) ||
+          !ptx::mbar_wait(ptx::smem_addr(&bars.v_full[vs]), (i / kVStages) & 1, abort_flag, p.err, kErrWaitMma,
+                          p.limit_ns)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after_sync();
+      const uint32_t vb = v_s0 + vs * kv_bytes;
+      const uint32_t a_p = tmem + s_col(i & 1, p.Bk);
+      for (int kk = 0; kk < p.Bk / 16; ++kk) {
+        ptx::mma_ts(tmem + kColO, a_p + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, half_bytes, 1024), idesc_o,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      ptx::mma_commit(ptx::smem_addr(&bars.v_empty[vs]));
+      ptx::mma_commit(ptx::smem_addr(&bars.pv_done));
+      if (i == nblk - 1) ptx::mma_commit(ptx::smem_addr(&bars.o_full));
+    }
+  }
+  // Every MMA issued above completes before TMEM is released.
+  ptx::mma_commit(ptx::smem_addr(&bars.drain));
+  drain_wait(ptx::smem_addr(&bars.drain), 0, p.err, p.limit_ns);
+}
+
+template <int D>
+__device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, int warp, int lane, int h, int f,
+                                                 int qt, int nblk, bool bounded, const FwdParams& p) {
+  volatile int* abort_flag = &bars.abort;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const int row = qt * kQTile + warp * 32 + lane;  // row inside the frame
+  const bool valid = row < p.T;
+  const int64_t grow = (int64_t)h * p.N + (int64_t)f * p.T + row;
+  const float sl2 = p.scale_log2;
+  // Row maximum in log2 units of the scaled logits.
+  float m_run = -INFINITY;
+  if (bounded) m_run = valid ? p.row_bound[grow] * kLog2e : 0.0f;
+  float l = 0.0f;
+  const int nchunks = p.Bk / 16;
+  bool ok = true;
+
+  for (int j = 0; j < nblk; ++j) {
+    const int buf = j & 1;
+    const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.s_full[buf]), (j >> 1) & 1, abort_flag, p.err,
+                                    kErrWaitSoftmax, p.limit_ns);
+    if (!__all_sync(0xffffffffu, got)) {
+      ok = false;
+      break;
+    }
+    ptx::tc_fence_after_sync();
+    const uint32_t sbase = tmem + lane_base + s_col(buf, p.Bk);
+
+    if (!bounded) {
+      float mx = -INFINITY;
+      for (int c = 0; c < nchunks; ++c) {
+        uint32_t r[16];
+        ptx::tmem_ld16(sbase + c * 16, r);
+        ptx::tmem_ld_wait(r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
+      }
+      const float cand = mx * sl2;
+      if (j == 0) {
+        m_run = cand;
+      } else {
+        const bool need = cand > m_run + kRescaleThreshold;
+        float alpha = 1.0f;
+        if (need) {
+          alpha = ptx::ex2(m_run - cand);
+          m_run = cand;
+          l *= alpha;
+        }
+        if (__any_sync(0xffffffffu, need)) {
+          // The accumulator may be rescaled only once P(j-1).V(j-1) is done.
+          const bool pv = ptx::mbar_wait(ptx::smem_addr(&bars.pv_done), (j - 1) & 1, abort_flag, p.err,
+                                         kErrWaitSoftmax, p.limit_ns);
+          if (!__all_sync(0xffffffffu, pv)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t r[16];
+            const uint32_t oaddr = tmem + lane_base + kColO + c * 16;
+            ptx::tmem_ld16(oaddr, r);
+            ptx::tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            ptx::tmem_st16(oaddr, r);
+          }
+        }
+      }
+    }
+
+    const float neg_m = -m_run;
+    for (int c = 0; c < nchunks; ++c) {
+      uint32_t r[16];
+      ptx::tmem_ld16(sbase + c * 16, r);
+      ptx::tmem_ld_wait(r);
+      uint32_t pk[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float p0 = ptx::ex2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m));
+        const float p1 = ptx::ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m));
+        l += p0 + p1;
+        pk[e] = ptx::pack_bf16x2(p0, p1);
+      }
+      // P columns [8c, 8c+8) lie below the S columns not yet read (>= 16(c+1)).
+      ptx::tmem_st8(sbase + c * 8, pk);
+    }
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before_sync();
+    ptx::mbar_arrive(ptx::smem_addr(&bars.p_full[buf]));
+  }
+
+  if (!ok) return;
+  const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.o_full), 0, abort_flag, p.err, kErrWaitSoftmax, p.limit_ns);
+  if (!__all_sync(0xffffffffu, got)) return;
+  ptx::tc_fence_after_sync();
+  const float inv = 1.0f / l;
+  uint16_t* orow = p.out + grow * D;
+#pragma unroll 1
+  for (int c = 0; c < D / 16; ++c) {
+    uint32_t r[16];
+    ptx::tmem_ld16(tmem + lane_base + kColO + c * 16, r);
+    ptx::tmem_ld_wait(r);
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      pk[e] = ptx::pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+    if (valid) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+      dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+  }
+  if (valid) p.lse[grow] = (m_run + ptx::lg2(l)) * kLn2;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attention_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Barriers bars;
+  const uint32_t tiles = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;  // 128B-swizzle atoms need 1 KB alignment
+  const uint32_t q_s = tiles;
+  const uint32_t k_s0 = q_s + kQTile * D * 2;
+  const uint32_t v_s0 = k_s0 + kKStages * (uint32_t)p.Bk * D * 2;
+
+  // A CTA of this launch (or an earlier one) already gave up on a wait: do
+  // nothing, the host reports FAS_ERR_TIMEOUT.
+  if (*reinterpret_cast<volatile unsigned int*>(p.err) != 0u) return;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int4 item = p.work[blockIdx.x];
+  const int h = item.x, f = item.y, qt = item.z, nblk = item.w;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_addr(&bars.q_full), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&bars.k_full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&bars.k_empty[s]), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&bars.v_full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&bars.v_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_addr(&bars.s_full[b]), 1);
+      ptx::mbar_init(ptx::smem_addr(&bars.p_full[b]), 4 * 32);
+    }
+    ptx::mbar_init(ptx::smem_addr(&bars.pv_done), 1);
+    ptx::mbar_init(ptx::smem_addr(&bars.o_full), 1);
+    ptx::mbar_init(ptx::smem_addr(&bars.drain), 1);
+    bars.abort = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(&bars.tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, bars, q_s, k_s0, v_s0, h, f, qt, p.table[f], p);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_issuer<D>(bars, tmem, q_s, k_s0, v_s0, nblk, p);
+  } else {
+    const bool bounded = p.mode == FAS_MODE_BOUNDED || (p.mode == FAS_MODE_AUTO && p.elig[h] != 0);
+    softmax_epilogue<D>(bars, tmem, warp, lane, h, f, qt, nblk, bounded, p);
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+__global__ void wait_selftest(unsigned int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_addr(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the bounded wait must give up and report.
+  if (threadIdx.x == 0)
+    ptx::mbar_wait(ptx::smem_addr(&bar), 0, &abort_flag, err, kErrWaitSelftest, limit_ns);
+  __syncthreads();
+}
+
+template <int D>
+size_t smem_bytes(int Bk) {
+  return 1024 + (size_t)kQTile * D * 2 + (size_t)(kKStages + kVStages) * Bk * D * 2;
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                     int grid, cudaStream_t st) {
+  const size_t smem = smem_bytes<D>(p.Bk);
+  cudaError_t e = cudaFuncSetAttribute(attention_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  attention_fwd<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FwdParams& p, int grid, cudaStream_t stream) {
+  if (d == 128) return launch_d<128>(tq, tk, tv, p, grid, stream);
+  if (d == 64) return launch_d<64>(tq, tk, tv, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_wait_selftest(unsigned int* err, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fas

@@ -1,0 +1,65 @@
+// Kernel launch interfaces (host side) and the parameter blocks they take.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fas {
+
+// Device error word bits.
+constexpr unsigned int kErrWaitProducer = 1u;
+constexpr unsigned int kErrWaitMma = 2u;
+constexpr unsigned int kErrWaitSoftmax = 4u;
+constexpr unsigned int kErrWaitDrain = 8u;
+constexpr unsigned int kErrWaitSelftest = 16u;
+
+// Bound on any single device-side wait in the attention kernel.
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+struct PrepassArgs {
+  const void* q;        // bf16 [H, N, d]
+  const void* k;        // bf16 [H, N, d]
+  const int4* table;    // [Nf] {start0, len0, start1, len1}
+  float* partial;       // [H, Nf, chunks, d]  per-chunk key sums
+  float* mu;            // [H, d]              mean key
+  float* fsum;          // [H, Nf, d]          per-frame key sums
+  float* mpart;         // [H, Nf, chunks]     per-chunk max centred key norm
+  float* frame_max;     // [H, Nf]             per-frame max centred key norm
+  float* mvis;          // [H, Nf]             max over the frames visible from f
+  float* kbarc;         // [H, Nf, d]          mean centred key visible from f
+  float* row_bound;     // [H, N]              m_i (natural-log units)
+  float* gpart;         // [H, Nf, chunks]     per-chunk max slack
+  float* stat;          // [H]                 max slack per head
+  uint8_t* elig;        // [H]
+  int64_t N;
+  int T, Nf, H, d, chunks;
+  float scale;          // 1/sqrt(d)
+};
+
+// Launches the six prepass kernels on `stream`; returns the number launched
+// (negative on a launch error).
+int launch_prepass(const PrepassArgs& a, cudaStream_t stream);
+
+struct FwdParams {
+  const int4* work;        // [n_work] {head, query frame, query tile, key blocks}
+  const int4* table;       // [Nf] {start0, len0, start1, len1}
+  const float* row_bound;  // [H, N] or null (online mode)
+  const uint8_t* elig;     // [H] or null (online mode)
+  uint16_t* out;           // bf16 [H, N, d]
+  float* lse;              // [H, N]
+  unsigned int* err;       // device error word
+  int64_t N;
+  int T;
+  int Bk;
+  int mode;                // FAS_MODE_*
+  float scale_log2;        // log2(e) / sqrt(d)
+  uint64_t limit_ns;
+};
+
+cudaError_t launch_attention(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FwdParams& p, int grid, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(unsigned int* err, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace fas

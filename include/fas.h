@@ -1,0 +1,162 @@
+/*
+ * fas.h — frame-aligned sparse attention for GB300 (sm_103a), C ABI.
+ *
+ * The operation (page "HeyGen x Google Cloud: Avatar IV on TPU",
+ * news.xcc.im/article/5328):
+ *
+ *   - section "Deleting the Mask": the queries of each video frame attend to
+ *     the keys of a window of nearby frames plus one global reference frame.
+ *     The live region snaps to frame boundaries, so key blocks whose size is a
+ *     multiple of 16 dividing the frame span are either fully visible or fully
+ *     hidden; one pass over the visible blocks covers the whole mask, with no
+ *     mask predicate, padding, second pass or merge.
+ *   - section "Unchaining the Softmax": the running maximum of online softmax
+ *     is replaced by a per-row upper bound (Cauchy-Schwarz: |q| times the
+ *     largest norm of the mean-centred keys the row can see).  Mean-centring
+ *     changes no output in exact arithmetic.  Heads whose bound is too loose
+ *     use the online-softmax path inside the same kernel.
+ *   - section "Proving the Pixels Didn't Change": the final product P.V runs
+ *     in bf16 on the matrix unit.
+ *
+ * Geometry.  T = frame_tokens, R0 = ref_frames, F = n_frames, Nf = R0 + F,
+ * N = Nf * T.  Token j belongs to frame j / T.  Frames 0..R0-1 are reference
+ * frames, R0..Nf-1 video frames in time order.  Query frame f sees
+ *   - every frame, if f < R0 (the reference is global both ways);
+ *   - frames 0..R0-1 and max(R0, f-r)..min(Nf-1, f+r), if f >= R0.
+ *
+ * Data layout (all device pointers, owned by the caller):
+ *   q, k, v, out : bf16, contiguous [H, N, d], base 16-byte aligned;
+ *   lse          : fp32, contiguous [H, N] (natural log of the sum of
+ *                  exp(s * q.k) over the visible keys, s = 1/sqrt(d)).
+ * Batch is folded into H: every head is independent.
+ *
+ * State.  The library holds one plan at a time (not thread-safe).  fas_plan
+ * owns the block table, the work list, the prepass statistics and a device
+ * error word; fas_free or the next fas_plan with other arguments releases
+ * them.  All device work is enqueued on the caller's stream (a cudaStream_t
+ * passed as void*; NULL = legacy default stream) and is asynchronous unless
+ * stated otherwise.
+ *
+ * Errors.  Every call returns FAS_OK (0) or a negative FAS_ERR_* code.
+ * Argument and order checks are synchronous and leave the state unchanged.
+ * Launch failures return FAS_ERR_CUDA.  A device-side wait that exceeds its
+ * bound sets the device error word; the next synchronising call (fas_status,
+ * or fas_prepass with elig_host) returns FAS_ERR_TIMEOUT.  No call traps or
+ * asserts on the device.
+ */
+#ifndef FAS_H_
+#define FAS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  FAS_OK = 0,
+  FAS_ERR_ARG = -1,         /* invalid shape or argument */
+  FAS_ERR_STATE = -2,       /* call out of order (no plan, no matching prepass) */
+  FAS_ERR_ALIGN = -3,       /* pointer not 16-byte aligned */
+  FAS_ERR_CUDA = -4,        /* CUDA runtime/driver error (no device, launch failure) */
+  FAS_ERR_TIMEOUT = -5,     /* a bounded device-side wait expired */
+  FAS_ERR_UNSUPPORTED = -6  /* valid request this build does not support */
+};
+
+enum {
+  FAS_MODE_AUTO = 0,    /* per head: bounded softmax if eligible, else online */
+  FAS_MODE_ONLINE = 1,  /* every head online softmax (running max + rescale) */
+  FAS_MODE_BOUNDED = 2  /* every head bounded softmax (ablation; loose heads may underflow) */
+};
+
+/* Per-head eligibility threshold: a head keeps the bounded softmax when the
+ * guaranteed gap between every row's bound and its true maximum is at most
+ * this many nats (e^-32 stays far above the fp32 underflow limit e^-87). */
+#define FAS_ELIG_SLACK_NATS 32.0f
+
+typedef struct {
+  int32_t block_k;       /* key block B_k: multiple of 16 that divides T */
+  int32_t q_tile;        /* query rows per work item (128); tiles never cross frames */
+  int32_t n_work;        /* work items = H * Nf * ceil(T / q_tile) */
+  int32_t total_frames;  /* Nf */
+  int64_t tokens;        /* N */
+  int64_t key_blocks;    /* sum over work items of visible key blocks */
+  double visible_flops;  /* 4*d per visible (query, key) pair, valid rows only */
+  const int32_t* host_table; /* library-owned, Nf x 4 int32 per query frame:
+                                start0, len0, start1, len1 (key tokens);
+                                len1 = 0 when the two ranges merge */
+} fas_plan_info;
+
+/* Build the block table and work list for one geometry ("Deleting the Mask",
+ * Fig. 3: blocks divide the frame's token span, so every block is full or
+ * skipped).  Requirements: T > 0, T % 16 == 0, F >= 1, R0 >= 0, r >= 0,
+ * H >= 1, d in {64, 128}.  B_k is the largest multiple of 16 dividing T that
+ * fits the kernel's on-chip budget (at most 192).  Allocates the library's
+ * device buffers (needs a CUDA device).  A call with the same arguments as
+ * the current plan is a no-op.  info (nullable) receives library-owned
+ * pointers valid until the next fas_plan or fas_free. */
+int fas_plan(int frame_tokens, int n_frames, int ref_frames, int window_radius,
+             int heads, int head_dim, fas_plan_info* info);
+
+/* fas_plan with an explicit key block size (block_k = 0: automatic).  A
+ * nonzero block_k must be a multiple of 16 dividing T and at most 192. */
+int fas_plan_ex(int frame_tokens, int n_frames, int ref_frames, int window_radius,
+                int heads, int head_dim, int block_k, fas_plan_info* info);
+
+/* Host-only planning: the same plan fas_plan_ex would build, written to the
+ * caller's buffers; touches no device and no library state.
+ *   table (nullable): Nf * 4 int32 (see fas_plan_info.host_table);
+ *   work  (nullable): n_work * 4 int32 per item: head, query frame,
+ *                     query tile, key block count; heaviest items first. */
+int fas_plan_describe(int frame_tokens, int n_frames, int ref_frames, int window_radius,
+                      int heads, int head_dim, int block_k, fas_plan_info* info,
+                      int32_t* table, int32_t* work);
+
+/* Prepass ("Unchaining the Softmax": precomputed norms, mean-centred keys).
+ * Reads q and k (device, bf16 [H, N, d]) and computes per head the mean key
+ * mu_h, per key frame the largest centred key norm, and per row
+ *   m_i = s q_i.mu_h + s |q_i| max_{visible frames g} max_{j in g} |k_j - mu_h|
+ * (an upper bound on the row's largest scaled logit), plus the eligibility
+ * statistic stat_h = max_i (b_i - s q_i.kbar_c(i)) where b_i is the centred
+ * bound and kbar_c(i) the mean centred key visible from row i; a head is
+ * eligible when stat_h <= FAS_ELIG_SLACK_NATS.  Needs a plan.  elig_host
+ * (nullable, H bytes, 1 = eligible): if set, the call synchronises the
+ * stream, copies the bits and reports device timeouts. */
+int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_host);
+
+/* Attention.  q, k, v: device bf16 [H, N, d]; out: device bf16 [H, N, d];
+ * lse: device fp32 [H, N].  Modes AUTO and BOUNDED need a prior fas_prepass
+ * on the same q and k (else FAS_ERR_STATE); ONLINE does not.  Every output
+ * row is written exactly once; out rows are rounded to bf16 (nearest even). */
+int fas_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                int mode, void* cuda_stream);
+
+/* Release every library-owned device buffer and forget the plan. */
+int fas_free(void);
+
+/* Synchronise the stream and report the device error word (FAS_OK or
+ * FAS_ERR_TIMEOUT); clears the word. */
+int fas_status(void* cuda_stream);
+
+/* Copy prepass results to host buffers (each nullable); synchronises the
+ * stream.  mu: H*d fp32; frame_max: H*Nf fp32 (largest centred key norm per
+ * key frame); stat: H fp32; elig: H bytes; row_bound: H*N fp32 (m_i). */
+int fas_prepass_readback(float* mu, float* frame_max, float* stat, uint8_t* elig,
+                         float* row_bound, void* cuda_stream);
+
+/* Self-test of the bounded device waits: launches one block that waits on
+ * an mbarrier nothing will complete, with the given limit in microseconds
+ * (1..1000000).  Expected result: FAS_ERR_TIMEOUT, with the context intact. */
+int fas_selftest_wait_timeout(int limit_us, void* cuda_stream);
+
+/* Kernel launches issued by the last fas_prepass / fas_forward call. */
+int fas_last_launch_count(void);
+
+/* Static description of a status code. */
+const char* fas_error_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FAS_H_ */

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path against the fp64 oracle, through the C ABI.
+
+Tolerances (bf16 inputs, fp32 accumulation, bf16 P in P.V as in "Proving the
+Pixels Didn't Change", bf16 output): max |out - oracle| <= 2e-2 and
+max |lse - oracle| <= 1e-3; eligibility bits bit-exact.  Small workloads are
+compared on every row; the full-size workloads on stratified sampled rows
+(every head, every query frame, frame edges, the ragged last query tile,
+reference rows, random interior rows), in the launch configuration the
+benchmark times.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import frame_aligned_sparse_gb300 as fas
+import workloads
+from oracle import reference as ref
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from frame_aligned_sparse_gb300 import build
+    build.build()
+    yield fas.load()
+    fas.fas_free()
+
+
+def to_dev(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def sample_rows(w, per_head_min=512, seed=0):
+    T, nf = w.frame_tokens, w.total_frames
+    rng = np.random.default_rng(seed)
+    rows = set()
+    last_tile = ((T - 1) // 128) * 128
+    for f in range(nf):
+        base = f * T
+        for r in (0, 1, 127, 128, T // 2, last_tile - 1, last_tile, T - 2, T - 1):
+            if 0 <= r < T:
+                rows.add(base + r)
+        rows.update((base + rng.choice(T, 8, replace=False)).tolist())
+    extra = per_head_min - len(rows)
+    if extra > 0:
+        rows.update(rng.choice(nf * T, extra + 64, replace=False).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+class Case:
+    """Inputs on host and device, the plan, and oracle results (cached)."""
+
+    def __init__(self, w, rows=None):
+        self.w = w
+        self.x = workloads.generate(w)
+        self.q, self.k, self.v = (to_dev(self.x[t]) for t in "qkv")
+        self.rows = rows
+        self._ref = None
+        self._st = None
+
+    def plan(self, block_k=0):
+        w = self.w
+        return fas.fas_plan(w.frame_tokens, w.n_frames, w.ref_frames, w.window_radius, w.heads, w.head_dim,
+                            block_k=block_k)
+
+    @property
+    def oracle(self):
+        if self._ref is None:
+            w = self.w
+            self._ref = ref.masked_attention(self.x["q"], self.x["k"], self.x["v"], w.frame_tokens, w.ref_frames,
+                                             w.window_radius, rows=self.rows)
+        return self._ref
+
+    @property
+    def stats(self):
+        if self._st is None:
+            w = self.w
+            self._st = ref.bound_statistics(self.x["q"], self.x["k"], w.frame_tokens, w.ref_frames,
+                                            w.window_radius)
+        return self._st
+
+    def run(self, mode, block_k=0):
+        self.plan(block_k)
+        elig = fas.fas_prepass(self.q, self.k, want_elig=True)
+        out, lse = fas.fas_forward(self.q, self.k, self.v, mode=mode)
+        assert fas.fas_status() == fas.FAS_OK
+        return elig, out, lse
+
+    def check(self, out, lse, label=""):
+        o = out.float().cpu().numpy()
+        l = lse.cpu().numpy()
+        if self.rows is not None:
+            o, l = o[:, self.rows], l[:, self.rows]
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(l)), label
+        d_out = np.abs(o - self.oracle["out"]).max()
+        d_lse = np.abs(l - self.oracle["lse"]).max()
+        assert d_out <= OUT_TOL, (label, "max |dout|", d_out)
+        assert d_lse <= LSE_TOL, (label, "max |dlse|", d_lse)
+        return d_out, d_lse
+
+
+_CASES = {}
+
+
+def case(name):
+    if name not in _CASES:
+        w = workloads.get(name)
+        rows = None if name in ("tiny", "mid") else sample_rows(w)
+        _CASES.clear()  # keep one large workload resident at a time
+        _CASES[name] = Case(w, rows)
+    return _CASES[name]
+
+
+def test_bounded_wait_selftest_reports_timeout():
+    assert fas.fas_selftest_wait_timeout(2000) == fas.FAS_ERR_TIMEOUT
+    # The context is still usable afterwards.
+    x = torch.arange(1024, device="cuda", dtype=torch.float32)
+    assert float(x.sum().item()) == 1023 * 1024 / 2
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_prepass_statistics(name):
+    c = case(name)
+    c.plan()
+    elig = fas.fas_prepass(c.q, c.k, want_elig=True)
+    got = fas.fas_prepass_readback(row_bound=True)
+    st = c.stats
+    np.testing.assert_allclose(got["mu"], st["mu"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["frame_max"], st["M"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["row_bound"], st["m"], rtol=1e-4, atol=1e-3)
+    np.testing.assert_allclose(got["stat"], st["stat"], rtol=1e-4, atol=1e-3)
+    assert np.array_equal(elig.astype(bool), st["elig"])
+    assert np.array_equal(got["elig"].astype(bool), st["elig"])
+
+
+@pytest.mark.parametrize("mode", ["auto", "online", "bounded"])
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_forward_full_rows(name, mode):
+    c = case(name)
+    _, out, lse = c.run(mode)
+    c.check(out, lse, f"{name}/{mode}")
+
+
+@pytest.mark.parametrize("name", ["720p", "1080p", "stress", "dense"])
+def test_forward_sampled_rows(name):
+    c = case(name)
+    results = {}
+    for mode in ("auto", "online"):
+        elig, out, lse = c.run(mode)
+        want = np.ones(c.w.heads, dtype=bool)
+        want[c.x["modified_heads"]] = False
+        assert np.array_equal(elig.astype(bool), want), (name, elig)
+        c.check(out, lse, f"{name}/{mode}")
+        results[mode] = (out.float(), lse.clone())
+    # Bounded and online softmax agree on the same (eligible) heads.
+    eligible = [h for h in range(c.w.heads) if h not in set(c.x["modified_heads"].tolist())]
+    a, b = results["auto"], results["online"]
+    assert (a[0][eligible] - b[0][eligible]).abs().max().item() <= OUT_TOL
+    assert (a[1][eligible] - b[1][eligible]).abs().max().item() <= LSE_TOL
+
+
+EDGE = [
+    # name, H, d, R0, F, T, r, sigma, seed, block_k
+    ("T16_r0", 2, 64, 1, 3, 16, 0, 2.0, 31, 0),
+    ("no_reference", 2, 128, 0, 5, 144, 1, 3.0, 32, 0),
+    ("two_references", 1, 128, 2, 4, 208, 1, 3.0, 33, 0),
+    ("single_frame", 1, 64, 1, 1, 256, 3, 2.0, 34, 0),
+    ("bk16_many_blocks", 1, 128, 1, 6, 400, 2, 3.0, 35, 16),
+    ("bk48_ragged", 3, 128, 1, 5, 336, 1, 3.0, 36, 48),
+    ("bk192", 1, 128, 1, 3, 384, 1, 3.0, 37, 192),
+    ("d64_wide_window", 2, 64, 1, 9, 240, 9, 2.0, 38, 0),
+]
+
+
+@pytest.mark.parametrize("spec", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_geometries(spec):
+    name, H, d, R0, F, T, r, sigma, seed, bk = spec
+    c = Case(workloads.Workload(name, H, d, R0, F, T, r, sigma, seed))
+    for mode in ("auto", "online"):
+        _, out, lse = c.run(mode, block_k=bk)
+        c.check(out, lse, f"{name}/{mode}")
+
+
+def test_outputs_are_bit_reproducible():
+    """Dual baseline ("Proving the Pixels Didn't Change"): two runs of the
+    same build on the same inputs must be identical."""
+    c = case("mid")
+    for mode in ("auto", "online"):
+        _, o1, l1 = c.run(mode)
+        o1, l1 = o1.clone(), l1.clone()
+        _, o2, l2 = c.run(mode)
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+        assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_argument_and_order_errors():
+    c = case("tiny")
+    c.plan()
+    lib = fas.load()
+    st = torch.cuda.current_stream().cuda_stream
+    lse = torch.empty(c.w.heads, c.w.tokens, device="cuda")
+    out = torch.empty_like(c.q)
+    # A different q than the one the prepass saw: state error.
+    fas.fas_prepass(c.q, c.k)
+    q2 = c.q.clone()
+    assert lib.fas_forward(q2.data_ptr(), c.k.data_ptr(), c.v.data_ptr(), out.data_ptr(), lse.data_ptr(), 0,
+                           st) == fas.FAS_ERR_STATE
+    # Online mode needs no prepass.
+    assert lib.fas_forward(q2.data_ptr(), c.k.data_ptr(), c.v.data_ptr(), out.data_ptr(), lse.data_ptr(), 1,
+                           st) == fas.FAS_OK
+    # Misaligned pointers.
+    assert lib.fas_prepass(c.q.data_ptr() + 2, c.k.data_ptr(), st, None) == fas.FAS_ERR_ALIGN
+    assert lib.fas_forward(c.q.data_ptr(), c.k.data_ptr(), c.v.data_ptr() + 2, out.data_ptr(), lse.data_ptr(), 1,
+                           st) == fas.FAS_ERR_ALIGN
+    # Bad mode.
+    assert lib.fas_forward(c.q.data_ptr(), c.k.data_ptr(), c.v.data_ptr(), out.data_ptr(), lse.data_ptr(), 7,
+                           st) == fas.FAS_ERR_ARG
+    assert fas.fas_status() == fas.FAS_OK
