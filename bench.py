@@ -378,7 +378,7 @@ def run_fas(args, w):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["fas", "reference"], default="fas")
     ap.add_argument("--workload", default="720p", choices=sorted(workloads.WORKLOADS))

@@ -213,7 +213,11 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   // Row maximum in log2 units of the scaled logits.
   float m_run = -INFINITY;
   if (bounded) m_run = valid ? p.row_bound[grow] * kLog2e : 0.0f;
-  float l = 0.0f;
+  // Two row sums: l of the fp32 probabilities (for the LSE) and lw of the
+  // bf16-rounded weights the P.V MMA actually uses (for normalising O, so
+  // the output is a convex combination of V rows even when the largest
+  // probability is not exactly 1 and its bf16 rounding is not negligible).
+  float l = 0.0f, lw = 0.0f;
   const int nchunks = p.Bk / 16;
   bool ok = true;
 
@@ -247,6 +251,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
           alpha = ptx::ex2(m_run - cand);
           m_run = cand;
           l *= alpha;
+          lw *= alpha;
         }
         if (__any_sync(0xffffffffu, need)) {
           // The accumulator may be rescaled only once P(j-1).V(j-1) is done.
@@ -283,6 +288,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
         const float p1 = ptx::ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m));
         l += p0 + p1;
         pk[e] = ptx::pack_bf16x2(p0, p1);
+        lw += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xFFFF0000u);
       }
       // P columns [8c, 8c+8) lie below the S columns not yet read (>= 16(c+1)).
       ptx::tmem_st8(sbase + c * 8, pk);
@@ -296,7 +302,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.o_full), 0, abort_flag, p.err, kErrWaitSoftmax, p.limit_ns);
   if (!__all_sync(0xffffffffu, got)) return;
   ptx::tc_fence_after_sync();
-  const float inv = 1.0f / l;
+  const float inv = 1.0f / lw;
   uint16_t* orow = p.out + grow * D;
 #pragma unroll 1
   for (int c = 0; c < D / 16; ++c) {

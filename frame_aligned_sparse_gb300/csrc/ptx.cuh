@@ -221,6 +221,38 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// Packed pair arithmetic (two fp32 lanes per instruction, sm_100 family).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// (d0, d1) = (a0, a1) * b + c, lane-wise.
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, uint64_t b, uint64_t c) {
+  asm("{\n\t.reg .b64 x, y;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "fma.rn.f32x2 y, x, %4, %5;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "l"(b), "l"(c));
+}
+
+// (a0, a1) += (b0, b1), lane-wise.
+__device__ __forceinline__ void add_f32x2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 x, x, y;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half.
