@@ -14,13 +14,22 @@
 //    tensor cores with fp32 accumulation.
 //
 // One CTA per work item (head h, query frame f, query tile of 128 rows).
-//   warps 0-3  softmax + epilogue; thread t owns row t of the tile, which is
-//              TMEM lane t (warp w reads lanes 32w..32w+31)
-//   warp 4     TMA producer: Q tile once, then K and V blocks into rings
-//   warp 5     TMEM allocator and tcgen05.mma issuer (one thread)
-// TMEM (512 columns): O at [0, d), S buffers at 128 and 128 + roundup32(Bk).
-// P (bf16) overwrites the first Bk/2 columns of its S buffer and feeds the
-// P.V MMA straight from TMEM.
+//   warps 0-7   softmax + epilogue in two warpgroups.  Thread (g, w, t) owns
+//               row 32(w%4) + t of the tile, i.e. TMEM lane 32(w%4) + t (warp
+//               w may only read lanes 32(w%4)..+31).  For bounded heads group
+//               g handles the blocks of S buffer g (even or odd blocks): the
+//               two groups ping-pong, each hiding the other's waits.  For
+//               online heads group 0 handles every block.
+//   warp 8      TMA producer of the Q tile and the K ring
+//   warp 9      TMA producer of the V ring (never waits behind K)
+//   warp 10     TMEM allocator and tcgen05.mma issuer (whole warp, one
+//               elected lane issues)
+// TMEM (512 columns): O at [0, d), S buffers at 128 and 128 + roundup32(Bk),
+// and, when Bk leaves room, the Q tile (bf16 pairs) at [448, 512) so that
+// S = Q.K^T reads its A operand from TMEM instead of shared memory.
+// The bf16 P of each 16-column chunk overwrites the first 8 columns of that
+// chunk (already read by the same thread) and feeds the P.V MMA straight
+// from TMEM, one 16-key MMA per chunk.
 // MMA issue order: S0, S1, PV0, S2, PV1, ...; the tensor pipe executes them
 // in order, so S(j+2) never overwrites P(j) before PV(j) has read it.
 
@@ -37,14 +46,20 @@
 namespace fas {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
+constexpr int kGroups = 2;  // softmax warpgroups, ping-pong over the S buffers
+constexpr int kHalfChunks = (kMaxBlockK / 16 + 1) / 2;  // S chunks in the first half of a block
+constexpr int kSoftmaxWarps = 4 * kGroups;
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kKProducerWarp = kSoftmaxWarps;
+constexpr int kVProducerWarp = kSoftmaxWarps + 1;
+constexpr int kMmaWarp = kSoftmaxWarps + 2;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+constexpr int kMaxStages = 4;  // per ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS0 = 128;
+constexpr uint32_t kColQ = 448;  // Q tile in TMEM (d/2 columns of bf16 pairs)
+constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier of all softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Online path: keep the current maximum until a block raises it by more than
@@ -53,10 +68,11 @@ constexpr float kRescaleThreshold = 8.0f;
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[kKStages];
-  uint64_t k_empty[kKStages];
-  uint64_t v_full[kVStages];
-  uint64_t v_empty[kVStages];
+  uint64_t q_tmem;  // Q copied into TMEM (used when Q lives in TMEM)
+  uint64_t k_full[kMaxStages];
+  uint64_t k_empty[kMaxStages];
+  uint64_t v_full[kMaxStages];
+  uint64_t v_empty[kMaxStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done;
@@ -64,11 +80,17 @@ struct Barriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  // Per-row partial sums of the softmax warpgroups, combined in the
+  // epilogue: [group][l, lw][row].
+  float red[kGroups][2][kQTile];
 };
 
-__device__ __forceinline__ uint32_t s_col(int buf, int Bk) {
+__host__ __device__ __forceinline__ uint32_t s_col(int buf, int Bk) {
   return buf == 0 ? kColS0 : kColS0 + ((uint32_t)(Bk + 31) & ~31u);
 }
+
+// Q fits in TMEM next to O and both S buffers.
+__host__ __device__ __forceinline__ bool q_fits_tmem(int Bk) { return s_col(1, Bk) + (uint32_t)Bk <= kColQ; }
 
 // Wait with no abort check (used only to drain in-flight copies and MMAs).
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsigned int* err, uint64_t limit) {
@@ -83,66 +105,86 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsign
   return true;
 }
 
+// One TMA ring (K or V): fills stage j % depth with block j of the visible
+// key ranges, after the consumer has released the stage's previous fill.
+// Stages below `dedicated` have their own slots; stage `dedicated` (when
+// depth > dedicated) is the Q slot, whose first fill waits until Q has been
+// copied out of it (`slot_free`).
 template <int D>
-__device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                         Barriers& bars, uint32_t q_s, uint32_t k_s0, uint32_t v_s0, int h, int f,
-                                         int qt, int4 rng, const FwdParams& p) {
-  volatile int* abort_flag = &bars.abort;
+__device__ __forceinline__ void ring_producer(const CUtensorMap* tm, uint64_t* full, uint64_t* empty, int depth,
+                                              int dedicated, uint32_t s0, uint32_t extra_slot, uint64_t* slot_free,
+                                              int h, int4 rng, volatile int* abort_flag, const FwdParams& p) {
   const uint32_t kv_bytes = (uint32_t)p.Bk * D * 2;
   const uint32_t half_bytes = (uint32_t)p.Bk * 128;
-  ptx::mbar_arrive_expect_tx(ptx::smem_addr(&bars.q_full), kQTile * D * 2);
-#pragma unroll
-  for (int half = 0; half < D / 64; ++half)
-    ptx::tma_load_4d(q_s + half * (kQTile * 128), tm_q, ptx::smem_addr(&bars.q_full), half * 64, qt * kQTile, f, h);
-
-  int k_fills[kKStages] = {0, 0};
-  int v_fills[kVStages] = {0, 0};
+  int fills[kMaxStages] = {0, 0, 0, 0};
   bool ok = true;
   int j = 0;
   for (int part = 0; part < 2 && ok; ++part) {
     const int start = part == 0 ? rng.x : rng.z;
     const int len = part == 0 ? rng.y : rng.w;
     for (int key = start; key < start + len; key += p.Bk, ++j) {
-      const int ks = j % kKStages, uk = j / kKStages;
-      if (uk >= 1 &&
-          !ptx::mbar_wait(ptx::smem_addr(&bars.k_empty[ks]), (uk - 1) & 1, abort_flag, p.err, kErrWaitProducer,
-                          p.limit_ns)) {
+      const int st = j % depth, u = j / depth;
+      bool got = true;
+      if (u >= 1)
+        got = ptx::mbar_wait<true>(ptx::smem_addr(&empty[st]), (u - 1) & 1, abort_flag, p.err, kErrWaitProducer,
+                                   p.limit_ns);
+      else if (st >= dedicated)
+        got = ptx::mbar_wait<true>(ptx::smem_addr(slot_free), 0, abort_flag, p.err, kErrWaitProducer, p.limit_ns);
+      if (!got) {
         ok = false;
         break;
       }
-      const uint32_t kfull = ptx::smem_addr(&bars.k_full[ks]);
-      ptx::mbar_arrive_expect_tx(kfull, kv_bytes);
+      const uint32_t dst = st < dedicated ? s0 + st * kv_bytes : extra_slot;
+      const uint32_t fb = ptx::smem_addr(&full[st]);
+      ptx::mbar_arrive_expect_tx(fb, kv_bytes);
 #pragma unroll
       for (int half = 0; half < D / 64; ++half)
-        ptx::tma_load_3d(k_s0 + ks * kv_bytes + half * half_bytes, tm_k, kfull, half * 64, key, h);
-      ++k_fills[ks];
-
-      const int vs = j % kVStages, uv = j / kVStages;
-      if (uv >= 1 &&
-          !ptx::mbar_wait(ptx::smem_addr(&bars.v_empty[vs]), (uv - 1) & 1, abort_flag, p.err, kErrWaitProducer,
-                          p.limit_ns)) {
-        ok = false;
-        break;
-      }
-      const uint32_t vfull = ptx::smem_addr(&bars.v_full[vs]);
-      ptx::mbar_arrive_expect_tx(vfull, kv_bytes);
-#pragma unroll
-      for (int half = 0; half < D / 64; ++half)
-        ptx::tma_load_3d(v_s0 + vs * kv_bytes + half * half_bytes, tm_v, vfull, half * 64, key, h);
-      ++v_fills[vs];
+        ptx::tma_load_3d(dst + half * half_bytes, tm, fb, half * 64, key, h);
+      ++fills[st];
     }
   }
   if (!ok) {
     // Let every copy this thread started land before the CTA exits.
-    drain_wait(ptx::smem_addr(&bars.q_full), 0, p.err, p.limit_ns);
-    for (int s = 0; s < kKStages; ++s)
-      if (k_fills[s] > 0) drain_wait(ptx::smem_addr(&bars.k_full[s]), (k_fills[s] - 1) & 1, p.err, p.limit_ns);
-    for (int s = 0; s < kVStages; ++s)
-      if (v_fills[s] > 0) drain_wait(ptx::smem_addr(&bars.v_full[s]), (v_fills[s] - 1) & 1, p.err, p.limit_ns);
+    for (int st = 0; st < depth; ++st)
+      if (fills[st] > 0) drain_wait(ptx::smem_addr(&full[st]), (fills[st] - 1) & 1, p.err, p.limit_ns);
   }
 }
 
+// O += P(i) . V(i) as NCH fully unrolled 16-key MMAs: M=128, N=d, K=16 each;
+// P from TMEM (chunk kk's P sits in the first 8 columns of its own 16 S
+// columns), V MN-major in shared memory.
+template <int D, int NCH>
+__device__ __forceinline__ void issue_pv(uint32_t d_o, uint32_t a_p, uint32_t vb, uint32_t half_bytes,
+                                         uint32_t idesc_o, bool first) {
+#pragma unroll
+  for (int kk = 0; kk < NCH; ++kk)
+    ptx::mma_ts_elect(d_o, a_p + kk * 16, ptx::smem_desc_sw128(vb + kk * 2048, half_bytes, 1024), idesc_o,
+                      (!first || kk > 0) ? 1u : 0u);
+}
+
 template <int D>
+__device__ __forceinline__ void issue_pv_any(int nch, uint32_t d_o, uint32_t a_p, uint32_t vb, uint32_t half_bytes,
+                                             uint32_t idesc_o, bool first) {
+  static_assert(kMaxBlockK / 16 <= 11, "extend the dispatch below");
+  switch (nch) {
+    case 1: issue_pv<D, 1>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 2: issue_pv<D, 2>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 3: issue_pv<D, 3>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 4: issue_pv<D, 4>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 5: issue_pv<D, 5>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 6: issue_pv<D, 6>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 7: issue_pv<D, 7>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 8: issue_pv<D, 8>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 9: issue_pv<D, 9>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    case 10: issue_pv<D, 10>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+    default: issue_pv<D, 11>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
+  }
+}
+
+// The MMA warp.  All 32 lanes run this loop with identical values (so the
+// descriptors stay warp-uniform) and one elected lane issues each MMA and
+// commit; every issue loop is fully unrolled.
+template <int D, bool kQTmem>
 __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32_t q_s, uint32_t k_s0,
                                            uint32_t v_s0, int nblk, const FwdParams& p) {
   volatile int* abort_flag = &bars.abort;
@@ -150,98 +192,208 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
   const uint32_t half_bytes = (uint32_t)p.Bk * 128;
   const uint32_t idesc_s = ptx::idesc_bf16_f32(kQTile, (uint32_t)p.Bk, false);
   const uint32_t idesc_o = ptx::idesc_bf16_f32(kQTile, D, true);
-  bool ok = ptx::mbar_wait(ptx::smem_addr(&bars.q_full), 0, abort_flag, p.err, kErrWaitMma, p.limit_ns);
+  const int nch = p.Bk / 16;
+  bool ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(kQTmem ? &bars.q_tmem : &bars.q_full), 0,
+                                                         abort_flag, p.err, kErrWaitMma, p.limit_ns));
+  // Ring positions (stage, phase parity) advanced incrementally.
+  int ks = 0, kph = 0, vs = 0, vph = 0;
   for (int j = 0; ok && j <= nblk; ++j) {
     if (j < nblk) {
-      // S(j) = Q . K(j)^T : M=128, N=Bk, K=d; both operands K-major, 128B swizzle.
-      const int ks = j % kKStages;
-      if (!ptx::mbar_wait(ptx::smem_addr(&bars.k_full[ks]), (j / kKStages) & 1, abort_flag, p.err, kErrWaitMma,
-                          p.limit_ns)) {
-        ok = false;
-        break;
-      }
+      // S(j) = Q . K(j)^T : M=128, N=Bk, K=d; K is K-major with 128B swizzle;
+      // Q comes from TMEM (bf16 pairs) or from shared memory like K.
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err,
+                                                        kErrWaitMma, p.limit_ns));
+      if (!ok) break;
       ptx::tc_fence_after_sync();
-      const uint32_t kb = k_s0 + ks * kv_bytes;
+      const uint32_t kb = ks < p.kd ? k_s0 + ks * kv_bytes : q_s;
       const uint32_t d_s = tmem + s_col(j & 1, p.Bk);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t a = q_s + (kk >> 2) * (kQTile * 128) + (kk & 3) * 32;
-        const uint32_t b = kb + (kk >> 2) * half_bytes + (kk & 3) * 32;
-        ptx::mma_ss(d_s, ptx::smem_desc_sw128(a, 16, 1024), ptx::smem_desc_sw128(b, 16, 1024), idesc_s,
-                    kk > 0 ? 1u : 0u);
+        const uint64_t bdesc = ptx::smem_desc_sw128(kb + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024);
+        if (kQTmem) {
+          ptx::mma_ts_elect(d_s, tmem + kColQ + kk * 8, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+        } else {
+          const uint32_t a = q_s + (kk >> 2) * (kQTile * 128) + (kk & 3) * 32;
+          ptx::mma_ss_elect(d_s, ptx::smem_desc_sw128(a, 16, 1024), bdesc, idesc_s, kk > 0 ? 1u : 0u);
+        }
       }
-      ptx::mma_commit(ptx::smem_addr(&bars.s_full[j & 1]));
-      ptx::mma_commit(ptx::smem_addr(&bars.k_empty[ks]));
+      ptx::mma_commit_elect(ptx::smem_addr(&bars.s_full[j & 1]));
+      ptx::mma_commit_elect(ptx::smem_addr(&bars.k_empty[ks]));
+      if (++ks == p.kst) {
+        ks = 0;
+        kph ^= 1;
+      }
     }
     if (j >= 1) {
-      // O += P(i) . V(i) : M=128, N=d, K=Bk; P from TMEM, V MN-major in smem.
       const int i = j - 1;
-      const int vs = i % kVStages;
-      if (!ptx::mbar_wait(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err, kErrWaitMma,
-                          p.limit_ns) ||
-          !ptx::mbar_wait(ptx::smem_addr(&bars.v_full[vs]), (i / kVStages) & 1, abort_flag, p.err, kErrWaitMma,
-                          p.limit_ns)) {
-        ok = false;
-        break;
-      }
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag,
+                                                        p.err, kErrWaitMma, p.limit_ns));
+      if (ok)
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(&bars.v_full[vs]), vph, abort_flag, p.err,
+                                                          kErrWaitMma, p.limit_ns));
+      if (!ok) break;
       ptx::tc_fence_after_sync();
-      const uint32_t vb = v_s0 + vs * kv_bytes;
-      const uint32_t a_p = tmem + s_col(i & 1, p.Bk);
-      for (int kk = 0; kk < p.Bk / 16; ++kk) {
-        ptx::mma_ts(tmem + kColO, a_p + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, half_bytes, 1024), idesc_o,
-                    (i > 0 || kk > 0) ? 1u : 0u);
+      issue_pv_any<D>(nch, tmem + kColO, tmem + s_col(i & 1, p.Bk), v_s0 + vs * kv_bytes, half_bytes, idesc_o,
+                      i == 0);
+      ptx::mma_commit_elect(ptx::smem_addr(&bars.v_empty[vs]));
+      ptx::mma_commit_elect(ptx::smem_addr(&bars.pv_done));
+      if (i == nblk - 1) ptx::mma_commit_elect(ptx::smem_addr(&bars.o_full));
+      if (++vs == p.vst) {
+        vs = 0;
+        vph ^= 1;
       }
-      ptx::mma_commit(ptx::smem_addr(&bars.v_empty[vs]));
-      ptx::mma_commit(ptx::smem_addr(&bars.pv_done));
-      if (i == nblk - 1) ptx::mma_commit(ptx::smem_addr(&bars.o_full));
     }
   }
   // Every MMA issued above completes before TMEM is released.
-  ptx::mma_commit(ptx::smem_addr(&bars.drain));
+  ptx::mma_commit_elect(ptx::smem_addr(&bars.drain));
   drain_wait(ptx::smem_addr(&bars.drain), 0, p.err, p.limit_ns);
 }
 
+// Copies this thread's Q row from the 128B-swizzled shared-memory tile into
+// TMEM as bf16 pairs (column c holds elements 2c, 2c+1), the A-operand layout
+// of tcgen05.mma.  In each 1 KB swizzle atom the 16-byte chunk index of row
+// t is XORed with t mod 8.
 template <int D>
-__device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, int warp, int lane, int h, int f,
-                                                 int qt, int nblk, bool bounded, const FwdParams& p) {
+__device__ __forceinline__ void stage_q_row(uint32_t q_s, uint32_t taddr, int trow) {
+#pragma unroll
+  for (int half = 0; half < D / 64; ++half) {
+    const uint32_t row_addr = q_s + half * (kQTile * 128) + trow * 128;
+    uint32_t w[2][16];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 x = ptx::ld_shared_v4(row_addr + ((uint32_t)(c ^ (trow & 7)) << 4));
+      w[c / 4][(c % 4) * 4 + 0] = x.x;
+      w[c / 4][(c % 4) * 4 + 1] = x.y;
+      w[c / 4][(c % 4) * 4 + 2] = x.z;
+      w[c / 4][(c % 4) * 4 + 3] = x.w;
+    }
+    ptx::tmem_st16(taddr + half * 32, w[0]);
+    ptx::tmem_st16(taddr + half * 32 + 16, w[1]);
+  }
+}
+
+// Softmax of one 16-column chunk held in registers: P = 2^(S*sl2 - m) (two
+// lanes per packed instruction), both row sums, P packed to bf16 pairs.
+__device__ __forceinline__ void exp_chunk(const uint32_t (&r)[16], uint64_t sl2, uint64_t neg_m, float& l0,
+                                          float& l1, float& w0, float& w1, uint32_t (&pk)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float x0, x1;
+    ptx::fma_f32x2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), sl2, neg_m);
+    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+    ptx::add_f32x2(l0, l1, p0, p1);
+    pk[e] = ptx::pack_bf16x2(p0, p1);
+    ptx::add_f32x2(w0, w1, __uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u));
+  }
+}
+
+// Issues the TMEM loads of chunks [c0, c0 + n) (n <= kHalfChunks).
+__device__ __forceinline__ void load_chunks(uint32_t sbase, int c0, int n, uint32_t (&r)[kHalfChunks][16]) {
+#pragma unroll
+  for (int u = 0; u < kHalfChunks; ++u)
+    if (u < n) ptx::tmem_ld16(sbase + (c0 + u) * 16, r[u]);
+}
+
+__device__ __forceinline__ void wait_chunks(int n, uint32_t (&r)[kHalfChunks][16]) {
+#pragma unroll
+  for (int u = 0; u < kHalfChunks; ++u)
+    if (u < n) ptx::tmem_ld_wait(r[u]);
+}
+
+// Row maximum of the block's raw scores (online path; one chunk at a time
+// to keep the fallback's registers low).
+__device__ __forceinline__ float block_max(uint32_t sbase, int nch) {
+  float mx = -INFINITY;
+  for (int c = 0; c < nch; ++c) {
+    uint32_t r[16];
+    ptx::tmem_ld16(sbase + c * 16, r);
+    ptx::tmem_ld_wait(r);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
+  }
+  return mx;
+}
+
+// P for one S block, in two phases (halves of the block's chunks).  All TMEM
+// loads of a phase go out before any of its stores: a TMEM load issued after
+// a TMEM store of the same thread waits for that store, so loading chunk by
+// chunk between stores would pay that wait once per chunk; here it is paid
+// once per block.  Each chunk's bf16 P lands in the first 8 columns of the
+// chunk's own S columns (already read).
+__device__ __forceinline__ void block_softmax(uint32_t sbase, int nch, uint64_t sl2, uint64_t neg_m, float& l0,
+                                              float& l1, float& w0, float& w1) {
+  const int na = (nch + 1) / 2;
+  for (int c0 = 0; c0 < nch; c0 += na) {
+    const int n = min(na, nch - c0);
+    uint32_t r[kHalfChunks][16];
+    load_chunks(sbase, c0, n, r);
+    wait_chunks(n, r);
+#pragma unroll
+    for (int u = 0; u < kHalfChunks; ++u)
+      if (u < n) {
+        if (u > 0) ptx::order_after(r[u], w1);
+        uint32_t pk[8];
+        exp_chunk(r[u], sl2, neg_m, l0, l1, w0, w1, pk);
+        ptx::tmem_st8(sbase + (c0 + u) * 16, pk);
+      }
+  }
+}
+
+// Softmax and epilogue for one thread: row `trow` of the tile.
+// Bounded heads: warpgroup g takes the blocks j with j % 2 == g, exactly the
+// blocks of S buffer g, so the two groups ping-pong and neither talks to the
+// other until the epilogue.  Online heads: warpgroup 0 takes every block (the
+// running maximum is a serial chain); warpgroup 1 joins for the epilogue.
+template <int D, bool kQTmem>
+__device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, uint32_t q_s, int warp, int lane,
+                                                 int h, int f, int qt, int nblk, bool bounded,
+                                                 const FwdParams& p) {
   volatile int* abort_flag = &bars.abort;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const int row = qt * kQTile + warp * 32 + lane;  // row inside the frame
+  const int g = warp / 4;
+  const int trow = (warp % 4) * 32 + lane;
+  const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
+  const int row = qt * kQTile + trow;  // row inside the frame
   const bool valid = row < p.T;
   const int64_t grow = (int64_t)h * p.N + (int64_t)f * p.T + row;
-  const float sl2 = p.scale_log2;
+  const int nch = p.Bk / 16;
+  const uint64_t sl2 = ptx::f32x2(p.scale_log2, p.scale_log2);
   // Row maximum in log2 units of the scaled logits.
   float m_run = -INFINITY;
   if (bounded) m_run = valid ? p.row_bound[grow] * kLog2e : 0.0f;
-  // Two row sums: l of the fp32 probabilities (for the LSE) and lw of the
-  // bf16-rounded weights the P.V MMA actually uses (for normalising O, so
-  // the output is a convex combination of V rows even when the largest
-  // probability is not exactly 1 and its bf16 rounding is not negligible).
-  float l = 0.0f, lw = 0.0f;
-  const int nchunks = p.Bk / 16;
+  // Two row sums, each kept as two interleaved partials: l of the fp32
+  // probabilities (for the LSE) and w of the bf16-rounded weights the P.V
+  // MMA actually uses (for normalising O, so the output is a convex
+  // combination of V rows even when the largest probability is not 1).
+  float l0 = 0.f, l1 = 0.f, w0 = 0.f, w1 = 0.f;
   bool ok = true;
 
-  for (int j = 0; j < nblk; ++j) {
+  if (kQTmem && g == 0) {
+    const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.q_full), 0, abort_flag, p.err, kErrWaitSoftmax, p.limit_ns);
+    ok = __all_sync(0xffffffffu, got);
+    if (ok) {
+      stage_q_row<D>(q_s, tmem + lane_base + kColQ, trow);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before_sync();
+      ptx::fence_proxy_async_smem();  // the Q slot is next written by TMA
+      ptx::mbar_arrive(ptx::smem_addr(&bars.q_tmem));
+    }
+  }
+
+  const int j0 = bounded ? g : 0;
+  const int jstep = bounded ? kGroups : 1;
+  const bool active = bounded || g == 0;
+  for (int j = j0; ok && active && j < nblk; j += jstep) {
     const int buf = j & 1;
     const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.s_full[buf]), (j >> 1) & 1, abort_flag, p.err,
                                     kErrWaitSoftmax, p.limit_ns);
-    if (!__all_sync(0xffffffffu, got)) {
-      ok = false;
-      break;
-    }
+    ok = __all_sync(0xffffffffu, got);
+    if (!ok) break;
     ptx::tc_fence_after_sync();
     const uint32_t sbase = tmem + lane_base + s_col(buf, p.Bk);
 
     if (!bounded) {
-      float mx = -INFINITY;
-      for (int c = 0; c < nchunks; ++c) {
-        uint32_t r[16];
-        ptx::tmem_ld16(sbase + c * 16, r);
-        ptx::tmem_ld_wait(r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
-      }
-      const float cand = mx * sl2;
+      const float mx = block_max(sbase, nch);
+      const float cand = mx * p.scale_log2;
       if (j == 0) {
         m_run = cand;
       } else {
@@ -250,88 +402,86 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
         if (need) {
           alpha = ptx::ex2(m_run - cand);
           m_run = cand;
-          l *= alpha;
-          lw *= alpha;
+          l0 *= alpha;
+          l1 *= alpha;
+          w0 *= alpha;
+          w1 *= alpha;
         }
         if (__any_sync(0xffffffffu, need)) {
           // The accumulator may be rescaled only once P(j-1).V(j-1) is done.
           const bool pv = ptx::mbar_wait(ptx::smem_addr(&bars.pv_done), (j - 1) & 1, abort_flag, p.err,
                                          kErrWaitSoftmax, p.limit_ns);
-          if (!__all_sync(0xffffffffu, pv)) {
-            ok = false;
-            break;
-          }
+          ok = __all_sync(0xffffffffu, pv);
+          if (!ok) break;
           ptx::tc_fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < D / 16; ++c) {
-            uint32_t r[16];
+            uint32_t o[16];
             const uint32_t oaddr = tmem + lane_base + kColO + c * 16;
-            ptx::tmem_ld16(oaddr, r);
-            ptx::tmem_ld_wait(r);
+            ptx::tmem_ld16(oaddr, o);
+            ptx::tmem_ld_wait(o);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            ptx::tmem_st16(oaddr, r);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st16(oaddr, o);
           }
         }
       }
     }
 
-    const float neg_m = -m_run;
-    for (int c = 0; c < nchunks; ++c) {
-      uint32_t r[16];
-      ptx::tmem_ld16(sbase + c * 16, r);
-      ptx::tmem_ld_wait(r);
-      uint32_t pk[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float p0 = ptx::ex2(fmaf(__uint_as_float(r[2 * e]), sl2, neg_m));
-        const float p1 = ptx::ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, neg_m));
-        l += p0 + p1;
-        pk[e] = ptx::pack_bf16x2(p0, p1);
-        lw += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xFFFF0000u);
-      }
-      // P columns [8c, 8c+8) lie below the S columns not yet read (>= 16(c+1)).
-      ptx::tmem_st8(sbase + c * 8, pk);
-    }
+    block_softmax(sbase, nch, sl2, ptx::f32x2(-m_run, -m_run), l0, l1, w0, w1);
     ptx::tmem_st_wait();
     ptx::tc_fence_before_sync();
     ptx::mbar_arrive(ptx::smem_addr(&bars.p_full[buf]));
   }
 
+  // Epilogue: combine the groups' row sums, then each group writes half of
+  // the output columns.  Every softmax thread reaches the named barrier.
+  if (ok) {
+    const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.o_full), 0, abort_flag, p.err, kErrWaitSoftmax, p.limit_ns);
+    ok = __all_sync(0xffffffffu, got);
+  }
+  bars.red[g][0][trow] = l0 + l1;
+  bars.red[g][1][trow] = w0 + w1;
+  ptx::named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
+  float l = 0.f, lw = 0.f;
+#pragma unroll
+  for (int q = 0; q < kGroups; ++q) {
+    l += bars.red[q][0][trow];
+    lw += bars.red[q][1][trow];
+  }
   if (!ok) return;
-  const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.o_full), 0, abort_flag, p.err, kErrWaitSoftmax, p.limit_ns);
-  if (!__all_sync(0xffffffffu, got)) return;
   ptx::tc_fence_after_sync();
   const float inv = 1.0f / lw;
   uint16_t* orow = p.out + grow * D;
+  constexpr int kOutChunks = D / 16 / kGroups;
 #pragma unroll 1
-  for (int c = 0; c < D / 16; ++c) {
-    uint32_t r[16];
-    ptx::tmem_ld16(tmem + lane_base + kColO + c * 16, r);
-    ptx::tmem_ld_wait(r);
+  for (int c = g * kOutChunks; c < (g + 1) * kOutChunks; ++c) {
+    uint32_t o[16];
+    ptx::tmem_ld16(tmem + lane_base + kColO + c * 16, o);
+    ptx::tmem_ld_wait(o);
     uint32_t pk[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      pk[e] = ptx::pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+      pk[e] = ptx::pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
     if (valid) {
       uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
       dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
   }
-  if (valid) p.lse[grow] = (m_run + ptx::lg2(l)) * kLn2;
+  if (valid && g == 0) p.lse[grow] = (m_run + ptx::lg2(l)) * kLn2;
 }
 
-template <int D>
+template <int D, bool kQTmem>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
   const uint32_t tiles = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;  // 128B-swizzle atoms need 1 KB alignment
-  const uint32_t q_s = tiles;
-  const uint32_t k_s0 = q_s + kQTile * D * 2;
-  const uint32_t v_s0 = k_s0 + kKStages * (uint32_t)p.Bk * D * 2;
+  const uint32_t q_s = tiles;  // Q tile, then (Q in TMEM) K stage kd
+  const uint32_t k_s0 = q_s + p.qslot_bytes;
+  const uint32_t v_s0 = k_s0 + (uint32_t)p.kd * p.Bk * D * 2;
 
   // A CTA of this launch (or an earlier one) already gave up on a wait: do
   // nothing, the host reports FAS_ERR_TIMEOUT.
@@ -343,17 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_addr(&bars.q_full), 1);
-    for (int s = 0; s < kKStages; ++s) {
+    ptx::mbar_init(ptx::smem_addr(&bars.q_tmem), 32 * 4);  // warpgroup 0
+    for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(ptx::smem_addr(&bars.k_full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&bars.k_empty[s]), 1);
-    }
-    for (int s = 0; s < kVStages; ++s) {
       ptx::mbar_init(ptx::smem_addr(&bars.v_full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&bars.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_addr(&bars.s_full[b]), 1);
-      ptx::mbar_init(ptx::smem_addr(&bars.p_full[b]), 4 * 32);
+      ptx::mbar_init(ptx::smem_addr(&bars.p_full[b]), 32 * 4);  // one warpgroup per block
     }
     ptx::mbar_init(ptx::smem_addr(&bars.pv_done), 1);
     ptx::mbar_init(ptx::smem_addr(&bars.o_full), 1);
@@ -371,13 +520,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after_sync();
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == kProducerWarp) {
-    if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, bars, q_s, k_s0, v_s0, h, f, qt, p.table[f], p);
+  if (warp == kKProducerWarp) {
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(ptx::smem_addr(&bars.q_full), kQTile * D * 2);
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half)
+        ptx::tma_load_4d(q_s + half * (kQTile * 128), &tm_q, ptx::smem_addr(&bars.q_full), half * 64, qt * kQTile, f,
+                         h);
+      ring_producer<D>(&tm_k, bars.k_full, bars.k_empty, p.kst, p.kd, k_s0, q_s, &bars.q_tmem, h, p.table[f],
+                       &bars.abort, p);
+      if (bars.abort) drain_wait(ptx::smem_addr(&bars.q_full), 0, p.err, p.limit_ns);
+    }
+  } else if (warp == kVProducerWarp) {
+    if (lane == 0)
+      ring_producer<D>(&tm_v, bars.v_full, bars.v_empty, p.vst, p.vst, v_s0, 0, nullptr, h, p.table[f], &bars.abort,
+                       p);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_issuer<D>(bars, tmem, q_s, k_s0, v_s0, nblk, p);
+    mma_issuer<D, kQTmem>(bars, tmem, q_s, k_s0, v_s0, nblk, p);
   } else {
     const bool bounded = p.mode == FAS_MODE_BOUNDED || (p.mode == FAS_MODE_AUTO && p.elig[h] != 0);
-    softmax_epilogue<D>(bars, tmem, warp, lane, h, f, qt, nblk, bounded, p);
+    softmax_epilogue<D, kQTmem>(bars, tmem, q_s, warp, lane, h, f, qt, nblk, bounded, p);
   }
 
   ptx::tc_fence_before_sync();
@@ -403,18 +565,33 @@ __global__ void wait_selftest(unsigned int* err, uint64_t limit_ns) {
   __syncthreads();
 }
 
-template <int D>
-size_t smem_bytes(int Bk) {
-  return 1024 + (size_t)kQTile * D * 2 + (size_t)(kKStages + kVStages) * Bk * D * 2;
-}
+constexpr size_t kSmemLimit = 232448;  // opt-in shared memory per block (sm_100 family)
 
-template <int D>
-cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                     int grid, cudaStream_t st) {
-  const size_t smem = smem_bytes<D>(p.Bk);
-  cudaError_t e = cudaFuncSetAttribute(attention_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <int D, bool kQTmem>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams p, int grid,
+                     cudaStream_t st) {
+  // Shared memory: [Q slot][kd K stages][vst V stages].  With Q in TMEM the
+  // Q slot (sized for a K stage too) becomes K stage kd once Q is copied.
+  const size_t kv_bytes = (size_t)p.Bk * D * 2;
+  const size_t q_bytes = (size_t)kQTile * D * 2;
+  const size_t qslot = kQTmem ? (kv_bytes > q_bytes ? kv_bytes : q_bytes) : q_bytes;
+  const size_t fixed = 1024 + qslot + sizeof(Barriers) + 256;
+  int n = (int)((kSmemLimit - fixed) / kv_bytes);
+  if (n > 2 * kMaxStages - 1) n = 2 * kMaxStages - 1;
+  if (n < 4) return cudaErrorInvalidValue;
+  int kd = n / 2;
+  if (kd > kMaxStages - 1) kd = kMaxStages - 1;
+  int vst = n - kd;
+  if (vst > kMaxStages) vst = kMaxStages;
+  p.kd = kd;
+  p.kst = kd + (kQTmem ? 1 : 0);
+  p.vst = vst;
+  p.qslot_bytes = (uint32_t)qslot;
+  const size_t smem = 1024 + qslot + (size_t)(kd + vst) * kv_bytes;
+  cudaError_t e = cudaFuncSetAttribute(attention_fwd<D, kQTmem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  attention_fwd<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+  attention_fwd<D, kQTmem><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -422,8 +599,11 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 cudaError_t launch_attention(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const FwdParams& p, int grid, cudaStream_t stream) {
-  if (d == 128) return launch_d<128>(tq, tk, tv, p, grid, stream);
-  if (d == 64) return launch_d<64>(tq, tk, tv, p, grid, stream);
+  const bool qt = q_fits_tmem(p.Bk);
+  if (d == 128) return qt ? launch_d<128, true>(tq, tk, tv, p, grid, stream)
+                          : launch_d<128, false>(tq, tk, tv, p, grid, stream);
+  if (d == 64) return qt ? launch_d<64, true>(tq, tk, tv, p, grid, stream)
+                         : launch_d<64, false>(tq, tk, tv, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

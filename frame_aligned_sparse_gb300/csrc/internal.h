@@ -7,7 +7,7 @@
 namespace fas {
 
 constexpr int kQTile = 128;        // query rows per work item (MMA M)
-constexpr int kMaxBlockK = 192;    // largest key block: two S buffers + O fit 512 TMEM columns
+constexpr int kMaxBlockK = 160;    // largest key block: TMEM (O, two S buffers, Q) and the softmax registers
 constexpr int kPrepassRows = 512;  // rows per prepass CTA (chunks never cross frames)
 
 struct HostPlan {

@@ -52,6 +52,9 @@ struct FwdParams {
   int64_t N;
   int T;
   int Bk;
+  int kst, vst;            // K and V ring depths (set by the launcher from the smem budget)
+  int kd;                  // K stages in their own slots; stage kd (if kst > kd) reuses the Q slot
+  uint32_t qslot_bytes;    // bytes of the shared-memory slot that first holds the Q tile
   int mode;                // FAS_MODE_*
   float scale_log2;        // log2(e) / sqrt(d)
   uint64_t limit_ns;

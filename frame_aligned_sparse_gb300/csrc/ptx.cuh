@@ -52,24 +52,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps (issuing nothing) until the phase completes or `hint_ns` passes,
+// instead of spinning and taking issue slots from the warps it shares a
+// scheduler with.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the completion of the phase with the given parity.
 // Returns false when the CTA-wide abort flag is raised, when another CTA has
 // already recorded an error, or when the wait exceeds limit_ns; in the last
 // case it raises the abort flag and records `code` in the device error word.
-// Never traps.
+// Never traps.  The abort flag, the clock and the (global) error word are
+// looked at only every 8 polls, so a completed phase is noticed promptly.
+// kSleep: poll with a suspend hint (for waits off the critical path, so
+// the waiting warp leaves the scheduler to the others).
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* err_word, unsigned int code,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (kSleep ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
+    if ((it & 7u) != 0u) continue;
     if (*abort_flag) return false;
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+      continue;
+    }
     if (*reinterpret_cast<volatile unsigned int*>(err_word) != 0u) {
       *abort_flag = 1;
       return false;
     }
-    if (global_timer_ns() - t0 > limit_ns) {
+    if (now - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(err_word, code);
       return false;
@@ -159,6 +185,40 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Whole-warp variants: every lane runs the issuing code with identical
+// (warp-uniform) operands and one elected lane issues.  Keeping the issue
+// loop convergent and fully unrolled is what lets the tensor pipe run at
+// full rate; a divergent single-lane loop issues several times slower.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
 // Arrive on the mbarrier once every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -221,6 +281,12 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(saddr));
+  return r;
+}
+
 // Packed pair arithmetic (two fp32 lanes per instruction, sm_100 family).
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
   uint64_t r;
@@ -247,6 +313,17 @@ __device__ __forceinline__ void add_f32x2(float& a0, float& a1, float b0, float 
       "mov.b64 {%0, %1}, x;\n\t}"
       : "+f"(a0), "+f"(a1)
       : "f"(b0), "f"(b1));
+}
+
+// Empty asm that makes the 16 registers of `r` depend on `after`: code that
+// uses `r` cannot be scheduled before `after` is computed.  Bounds how far the
+// compiler interleaves independent unrolled chunks (and so their registers).
+__device__ __forceinline__ void order_after(uint32_t (&r)[16], float after) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               : "f"(after));
 }
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {

@@ -91,7 +91,7 @@ typedef struct {
  * Fig. 3: blocks divide the frame's token span, so every block is full or
  * skipped).  Requirements: T > 0, T % 16 == 0, F >= 1, R0 >= 0, r >= 0,
  * H >= 1, d in {64, 128}.  B_k is the largest multiple of 16 dividing T that
- * fits the kernel's on-chip budget (at most 192).  Allocates the library's
+ * fits the kernel's on-chip budget (at most 160).  Allocates the library's
  * device buffers (needs a CUDA device).  A call with the same arguments as
  * the current plan is a no-op.  info (nullable) receives library-owned
  * pointers valid until the next fas_plan or fas_free. */
@@ -99,7 +99,7 @@ int fas_plan(int frame_tokens, int n_frames, int ref_frames, int window_radius,
              int heads, int head_dim, fas_plan_info* info);
 
 /* fas_plan with an explicit key block size (block_k = 0: automatic).  A
- * nonzero block_k must be a multiple of 16 dividing T and at most 192. */
+ * nonzero block_k must be a multiple of 16 dividing T and at most 160. */
 int fas_plan_ex(int frame_tokens, int n_frames, int ref_frames, int window_radius,
                 int heads, int head_dim, int block_k, fas_plan_info* info);
 

@@ -175,7 +175,7 @@ EDGE = [
     ("single_frame", 1, 64, 1, 1, 256, 3, 2.0, 34, 0),
     ("bk16_many_blocks", 1, 128, 1, 6, 400, 2, 3.0, 35, 16),
     ("bk48_ragged", 3, 128, 1, 5, 336, 1, 3.0, 36, 48),
-    ("bk192", 1, 128, 1, 3, 384, 1, 3.0, 37, 192),
+    ("bk160", 1, 128, 1, 3, 320, 1, 3.0, 37, 160),
     ("d64_wide_window", 2, 64, 1, 9, 240, 9, 2.0, 38, 0),
 ]
 

@@ -74,7 +74,7 @@ def test_plan_covers_mask_exactly(geo):
     Bk = info.block_k
     nf = R0 + F
     N = nf * T
-    assert Bk % 16 == 0 and T % Bk == 0 and 16 <= Bk <= 192
+    assert Bk % 16 == 0 and T % Bk == 0 and 16 <= Bk <= 160
     assert info.tokens == N and info.total_frames == nf
     for f in range(nf):
         blocks = expand_blocks(table[f], Bk)
@@ -102,8 +102,8 @@ def test_plan_covers_mask_exactly(geo):
 
 
 def test_block_size_choice_matches_frame_spans():
-    # Largest multiple of 16 dividing T within the on-chip budget (<= 192).
-    for T, want in ((48, 48), (880, 176), (3600, 144), (8160, 160), (16, 16), (4096, 128), (192, 192), (400, 80)):
+    # Largest multiple of 16 dividing T within the on-chip budget (<= 160).
+    for T, want in ((48, 48), (880, 80), (3600, 144), (8160, 160), (16, 16), (4096, 128), (192, 96), (352, 32), (320, 160), (400, 80)):
         info, _, _ = fas.fas_plan_describe(T, 3, 1, 1, 1, 128)
         assert info.block_k == want, (T, info.block_k)
     info, _, _ = fas.fas_plan_describe(3600, 3, 1, 1, 1, 128, block_k=48)
@@ -113,7 +113,7 @@ def test_block_size_choice_matches_frame_spans():
 @pytest.mark.parametrize("args", [
     (0, 8, 1, 1, 2, 64, 0), (40, 8, 1, 1, 2, 64, 0), (48, 0, 1, 1, 2, 64, 0), (48, 8, -1, 1, 2, 64, 0),
     (48, 8, 1, -1, 2, 64, 0), (48, 8, 1, 1, 0, 64, 0), (48, 8, 1, 1, 2, 96, 0), (48, 8, 1, 1, 2, 64, 32),
-    (48, 8, 1, 1, 2, 64, 8), (3840, 8, 1, 1, 2, 64, 240),
+    (48, 8, 1, 1, 2, 64, 8), (3840, 8, 1, 1, 2, 64, 240), (384, 8, 1, 1, 2, 64, 192), (352, 8, 1, 1, 2, 64, 176),
 ])
 def test_bad_arguments_are_rejected(args):
     lib = fas.load()
