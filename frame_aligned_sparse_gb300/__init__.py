@@ -24,9 +24,12 @@ __all__ = [
     "FasError", "PlanInfo", "MODES", "library_path", "load",
     "fas_plan", "fas_plan_describe", "fas_prepass", "fas_forward", "fas_free",
     "fas_status", "fas_prepass_readback", "fas_selftest_wait_timeout", "fas_last_launch_count",
+    "fas_prepass_noalloc",
 ]
 
 FAS_OK, FAS_ERR_ARG, FAS_ERR_STATE, FAS_ERR_ALIGN, FAS_ERR_CUDA, FAS_ERR_TIMEOUT, FAS_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+FAS_ERR_SCRATCH = -7
+FAS_NOALLOC_SCRATCH_BYTES = 4 << 20
 MODES = {"auto": 0, "online": 1, "bounded": 2}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +84,8 @@ _SIGS = {
     "fas_prepass_readback": (ctypes.c_int, [ctypes.c_void_p] * 6),
     "fas_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p]),
     "fas_last_launch_count": (ctypes.c_int, []),
+    "fas_prepass_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 6 +
+                            [ctypes.c_void_p] * 4),
     "fas_error_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -231,6 +236,25 @@ def fas_prepass_readback(stream=None, row_bound: bool = False) -> dict:
 
 def fas_selftest_wait_timeout(limit_us: int, stream=None) -> int:
     return load().fas_selftest_wait_timeout(limit_us, _stream_handle(stream))
+
+
+def fas_prepass_noalloc(q, k, frame_tokens: int, n_frames: int, ref_frames: int, window_radius: int,
+                        row_bound, stat, elig, stream=None) -> None:
+    """The prepass without any allocation (see ``fas_prepass_noalloc`` in
+    fas.h): the caller provides every output buffer; the library uses a fixed
+    device array as scratch.  q, k: bf16 [H, N, d]; row_bound: fp32 [H, N];
+    stat: fp32 [H]; elig: uint8 [H] (all CUDA tensors)."""
+    import torch
+    H, N, d = q.shape
+    _check_tensor("q", q, (H, N, d), torch.bfloat16)
+    _check_tensor("k", k, (H, N, d), torch.bfloat16)
+    _check_tensor("row_bound", row_bound, (H, N), torch.float32)
+    _check_tensor("stat", stat, (H,), torch.float32)
+    _check_tensor("elig", elig, (H,), torch.uint8)
+    rc = load().fas_prepass_noalloc(q.data_ptr(), k.data_ptr(), frame_tokens, n_frames, ref_frames, window_radius,
+                                    H, d, row_bound.data_ptr(), stat.data_ptr(), elig.data_ptr(),
+                                    _stream_handle(stream))
+    _check("fas_prepass_noalloc", rc)
 
 
 def fas_last_launch_count() -> int:

@@ -347,6 +347,7 @@ const char* fas_error_string(int status) {
     case FAS_ERR_CUDA: return "CUDA error";
     case FAS_ERR_TIMEOUT: return "device-side wait exceeded its bound";
     case FAS_ERR_UNSUPPORTED: return "unsupported";
+    case FAS_ERR_SCRATCH: return "problem larger than the fixed scratch of fas_prepass_noalloc";
     default: return "unknown status";
   }
 }

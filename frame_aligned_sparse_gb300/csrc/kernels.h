@@ -41,6 +41,11 @@ struct PrepassArgs {
 // (negative on a launch error).
 int launch_prepass(const PrepassArgs& a, cudaStream_t stream);
 
+// The same six kernels, with the window statistics computed from the frame
+// rule instead of the plan's block table (no library state needed).  The
+// table pointer in `a` is not used.
+int launch_prepass_rule(const PrepassArgs& a, int ref_frames, int window_radius, cudaStream_t stream);
+
 struct FwdParams {
   const int4* work;        // [n_work] {head, query frame, query tile, key blocks}
   const int4* table;       // [Nf] {start0, len0, start1, len1}

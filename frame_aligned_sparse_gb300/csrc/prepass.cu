@@ -198,6 +198,45 @@ __global__ void __launch_bounds__(D) window_stats(const float* __restrict__ mpar
   }
 }
 
+// (4') The same statistics with the visible frames taken straight from the
+// frame rule (reference frames global both ways, window clipped to the
+// video frames) instead of a block table in device memory.
+template <int D>
+__global__ void __launch_bounds__(D) window_stats_rule(const float* __restrict__ mpart,
+                                                       const float* __restrict__ fsum, const float* __restrict__ mu,
+                                                       float* __restrict__ frame_max, float* __restrict__ mvis,
+                                                       float* __restrict__ kbarc, int T, int Nf, int chunks, int R0,
+                                                       int r) {
+  const int h = blockIdx.x, e = threadIdx.x;
+  for (int g = e; g < Nf; g += D) {
+    float mx = 0.f;
+    for (int c = 0; c < chunks; ++c) mx = fmaxf(mx, mpart[((int64_t)h * Nf + g) * chunks + c]);
+    frame_max[(int64_t)h * Nf + g] = mx;
+  }
+  __syncthreads();
+  const float mue = mu[(int64_t)h * D + e];
+  for (int f = 0; f < Nf; ++f) {
+    // Visible frames: [0, a) and [b, c).
+    int a, b, c;
+    if (f < R0) {
+      a = Nf; b = Nf; c = Nf;
+    } else {
+      a = R0; b = max(R0, f - r); c = min(Nf - 1, f + r) + 1;
+    }
+    float acc = 0.f, mx = 0.f;
+    for (int g = 0; g < a; ++g) {
+      acc += fsum[((int64_t)h * Nf + g) * D + e];
+      mx = fmaxf(mx, frame_max[(int64_t)h * Nf + g]);
+    }
+    for (int g = b; g < c; ++g) {
+      acc += fsum[((int64_t)h * Nf + g) * D + e];
+      mx = fmaxf(mx, frame_max[(int64_t)h * Nf + g]);
+    }
+    kbarc[((int64_t)h * Nf + f) * D + e] = acc / (float)((a + c - b) * T) - mue;
+    if (e == 0) mvis[(int64_t)h * Nf + f] = mx;
+  }
+}
+
 // (5) Per row: m_i, and the per-chunk max of the slack G_i.
 template <int D>
 __global__ void __launch_bounds__(kPrepassThreads) query_bounds(const uint4* __restrict__ q,
@@ -296,7 +335,38 @@ int launch_prepass_d(const PrepassArgs& a, cudaStream_t st) {
   return n;
 }
 
+template <int D>
+int launch_prepass_rule_d(const PrepassArgs& a, int R0, int r, cudaStream_t st) {
+  const dim3 grid(a.chunks, a.Nf, a.H);
+  const uint4* q = static_cast<const uint4*>(a.q);
+  const uint4* k = static_cast<const uint4*>(a.k);
+  int n = 0;
+  key_chunk_sums<D><<<grid, kPrepassThreads, 0, st>>>(k, a.partial, a.N, a.T, a.Nf, a.chunks);
+  ++n;
+  key_frame_sums<D><<<a.H, D, 0, st>>>(a.partial, a.fsum, a.mu, a.N, a.Nf, a.chunks);
+  ++n;
+  key_centred_max<D><<<grid, kPrepassThreads, 0, st>>>(k, a.mu, a.mpart, a.N, a.T, a.Nf, a.chunks);
+  ++n;
+  window_stats_rule<D><<<a.H, D, 0, st>>>(a.mpart, a.fsum, a.mu, a.frame_max, a.mvis, a.kbarc, a.T, a.Nf, a.chunks,
+                                          R0, r);
+  ++n;
+  query_bounds<D><<<grid, kPrepassThreads, 0, st>>>(q, a.mu, a.mvis, a.kbarc, a.row_bound, a.gpart, a.N, a.T,
+                                                    a.Nf, a.chunks, a.scale);
+  ++n;
+  const int blocks = (a.H + 255) / 256;
+  eligibility<<<blocks, 256, 0, st>>>(a.gpart, a.stat, a.elig, a.H, a.Nf * a.chunks);
+  ++n;
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  return n;
+}
+
 }  // namespace
+
+int launch_prepass_rule(const PrepassArgs& a, int ref_frames, int window_radius, cudaStream_t stream) {
+  if (a.d == 128) return launch_prepass_rule_d<128>(a, ref_frames, window_radius, stream);
+  if (a.d == 64) return launch_prepass_rule_d<64>(a, ref_frames, window_radius, stream);
+  return -1;
+}
 
 int launch_prepass(const PrepassArgs& a, cudaStream_t stream) {
   if (a.d == 128) return launch_prepass_d<128>(a, stream);

@@ -1,0 +1,104 @@
+// fas_prepass_noalloc: the prepass with its scratch in a fixed static device
+// array, for callers that cannot allocate device memory.  See include/fas.h.
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fas.h"
+#include "internal.h"
+#include "kernels.h"
+
+namespace fas {
+namespace {
+
+// The scratch.  In host code `g_noalloc_scratch` is only a stand-in for the
+// symbol; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FAS_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_addr_mutex;
+void* g_addr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch on the current device (looked up once).
+int scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return FAS_ERR_CUDA;
+  if (dev >= kMaxDevices) return FAS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_addr_mutex);
+  if (g_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FAS_ERR_CUDA;
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
+  return FAS_OK;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+}  // namespace
+}  // namespace fas
+
+extern "C" int fas_prepass_noalloc(const void* q, const void* k, int frame_tokens, int n_frames, int ref_frames,
+                                   int window_radius, int heads, int head_dim, float* row_bound, float* stat,
+                                   uint8_t* elig, void* cuda_stream) {
+  using namespace fas;
+  const int T = frame_tokens, F = n_frames, R0 = ref_frames, r = window_radius, H = heads, d = head_dim;
+  if (T <= 0 || T % 16 != 0 || F < 1 || R0 < 0 || r < 0 || H < 1 || (d != 64 && d != 128)) return FAS_ERR_ARG;
+  const int64_t Nf = (int64_t)R0 + F;
+  const int64_t N = Nf * T;
+  if (N > (int64_t)INT32_MAX || (int64_t)H * N > (int64_t)INT32_MAX) return FAS_ERR_ARG;
+  if (!q || !k || !row_bound || !stat || !elig) return FAS_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(k) & 15u) ||
+      (reinterpret_cast<uintptr_t>(row_bound) & 3u) || (reinterpret_cast<uintptr_t>(stat) & 3u))
+    return FAS_ERR_ALIGN;
+
+  // Scratch layout (fp32): per-chunk key sums, mean key, frame sums,
+  // per-chunk and per-frame max centred norms, window maxima, window mean
+  // centred keys, per-chunk slack maxima.
+  const int chunks = (T + kPrepassRows - 1) / kPrepassRows;
+  const size_t hs = (size_t)H, nf = (size_t)Nf, cs = (size_t)chunks, ds = (size_t)d;
+  const size_t sizes[8] = {hs * nf * cs * ds * 4, hs * ds * 4, hs * nf * ds * 4, hs * nf * cs * 4,
+                           hs * nf * 4,           hs * nf * 4, hs * nf * ds * 4, hs * nf * cs * 4};
+  size_t total = 0;
+  for (size_t b : sizes) total += round256(b);
+  if (total > (size_t)FAS_NOALLOC_SCRATCH_BYTES) return FAS_ERR_SCRATCH;
+
+  void* base = nullptr;
+  const int rc = scratch_address(&base);
+  if (rc != FAS_OK) return rc;
+  float* part[8];
+  size_t off = 0;
+  for (int i = 0; i < 8; ++i) {
+    part[i] = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + off);
+    off += round256(sizes[i]);
+  }
+
+  PrepassArgs a;
+  a.q = q;
+  a.k = k;
+  a.table = nullptr;
+  a.partial = part[0];
+  a.mu = part[1];
+  a.fsum = part[2];
+  a.mpart = part[3];
+  a.frame_max = part[4];
+  a.mvis = part[5];
+  a.kbarc = part[6];
+  a.gpart = part[7];
+  a.row_bound = row_bound;
+  a.stat = stat;
+  a.elig = elig;
+  a.N = N;
+  a.T = T;
+  a.Nf = (int)Nf;
+  a.H = H;
+  a.d = d;
+  a.chunks = chunks;
+  a.scale = (float)(1.0 / sqrt((double)d));
+  const int n = launch_prepass_rule(a, R0, r, static_cast<cudaStream_t>(cuda_stream));
+  return n > 0 ? FAS_OK : FAS_ERR_CUDA;
+}

@@ -60,7 +60,8 @@ enum {
   FAS_ERR_ALIGN = -3,       /* pointer not 16-byte aligned */
   FAS_ERR_CUDA = -4,        /* CUDA runtime/driver error (no device, launch failure) */
   FAS_ERR_TIMEOUT = -5,     /* a bounded device-side wait expired */
-  FAS_ERR_UNSUPPORTED = -6  /* valid request this build does not support */
+  FAS_ERR_UNSUPPORTED = -6, /* valid request this build does not support */
+  FAS_ERR_SCRATCH = -7      /* problem needs more than fas_prepass_noalloc's fixed scratch */
 };
 
 enum {
@@ -148,6 +149,37 @@ int fas_prepass_readback(float* mu, float* frame_max, float* stat, uint8_t* elig
  * an mbarrier nothing will complete, with the given limit in microseconds
  * (1..1000000).  Expected result: FAS_ERR_TIMEOUT, with the context intact. */
 int fas_selftest_wait_timeout(int limit_us, void* cuda_stream);
+
+/* Bytes of the fixed device array that fas_prepass_noalloc uses as scratch. */
+#define FAS_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* fas_prepass for callers that cannot allocate device memory.  (The pages
+ * have no counterpart; this is a deployment convenience.)  Some callers own
+ * all device memory themselves: a serving process that reserves the GPU's
+ * memory in its own pool at start-up and hands libraries only pre-sized
+ * buffers, or a per-chunk streaming loop that must not stall on
+ * cudaMalloc/cudaFree, which can synchronise the device.  This call needs no
+ * plan and allocates nothing: its scratch is a fixed array of
+ * FAS_NOALLOC_SCRATCH_BYTES in device memory that the library image holds on
+ * every GPU that loads it, until the process exits.
+ *   q, k       : device bf16 [H, N, d] (as for fas_prepass), 16-byte aligned;
+ *   row_bound  : device fp32 [H, N], receives m_i (as fas_prepass_readback);
+ *   stat       : device fp32 [H], receives stat_h;
+ *   elig       : device uint8 [H], receives the eligibility bits.
+ * The geometry arguments follow fas_plan.  The scratch needed is about
+ * 4 * H * Nf * (ceil(T/512) * d + 2 * d) bytes; a geometry that does not fit
+ * returns FAS_ERR_SCRATCH before any device work (e.g. 720p and 1080p SR
+ * chunks with H = 24, d = 128 fit; H = 48 at 720p does not).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and leave their
+ * values in it (every element is written before it is read, so nothing
+ * needs clearing): calls that may overlap on the GPU — other streams, other
+ * host threads — race and must be serialised by the caller.  Asynchronous
+ * on cuda_stream; launch errors return FAS_ERR_CUDA. */
+int fas_prepass_noalloc(const void* q, const void* k, int frame_tokens, int n_frames, int ref_frames,
+                        int window_radius, int heads, int head_dim, float* row_bound, float* stat,
+                        uint8_t* elig, void* cuda_stream);
 
 /* Kernel launches issued by the last fas_prepass / fas_forward call. */
 int fas_last_launch_count(void);
