@@ -32,6 +32,10 @@
 // from TMEM, one 16-key MMA per chunk.
 // MMA issue order: S0, S1, PV0, S2, PV1, ...; the tensor pipe executes them
 // in order, so S(j+2) never overwrites P(j) before PV(j) has read it.
+// The kernel is instantiated per number of 16-key chunks in a block (the
+// plan fixes the block size), so every loop over chunks is unrolled with no
+// run-time predicate around the warp-collective tcgen05 loads, stores and
+// MMAs: predicated forms of them measured ~20% slower.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -47,7 +51,6 @@ namespace fas {
 namespace {
 
 constexpr int kGroups = 2;  // softmax warpgroups, ping-pong over the S buffers
-constexpr int kHalfChunks = (kMaxBlockK / 16 + 1) / 2;  // S chunks in the first half of a block
 constexpr int kSoftmaxWarps = 4 * kGroups;
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kKProducerWarp = kSoftmaxWarps;
@@ -85,12 +88,12 @@ struct Barriers {
   float red[kGroups][2][kQTile];
 };
 
-__host__ __device__ __forceinline__ uint32_t s_col(int buf, int Bk) {
+__host__ __device__ constexpr uint32_t s_col(int buf, int Bk) {
   return buf == 0 ? kColS0 : kColS0 + ((uint32_t)(Bk + 31) & ~31u);
 }
 
 // Q fits in TMEM next to O and both S buffers.
-__host__ __device__ __forceinline__ bool q_fits_tmem(int Bk) { return s_col(1, Bk) + (uint32_t)Bk <= kColQ; }
+__host__ __device__ constexpr bool q_fits_tmem(int Bk) { return s_col(1, Bk) + (uint32_t)Bk <= kColQ; }
 
 // Wait with no abort check (used only to drain in-flight copies and MMAs).
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsigned int* err, uint64_t limit) {
@@ -162,37 +165,17 @@ __device__ __forceinline__ void issue_pv(uint32_t d_o, uint32_t a_p, uint32_t vb
                       (!first || kk > 0) ? 1u : 0u);
 }
 
-template <int D>
-__device__ __forceinline__ void issue_pv_any(int nch, uint32_t d_o, uint32_t a_p, uint32_t vb, uint32_t half_bytes,
-                                             uint32_t idesc_o, bool first) {
-  static_assert(kMaxBlockK / 16 <= 11, "extend the dispatch below");
-  switch (nch) {
-    case 1: issue_pv<D, 1>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 2: issue_pv<D, 2>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 3: issue_pv<D, 3>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 4: issue_pv<D, 4>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 5: issue_pv<D, 5>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 6: issue_pv<D, 6>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 7: issue_pv<D, 7>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 8: issue_pv<D, 8>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 9: issue_pv<D, 9>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    case 10: issue_pv<D, 10>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-    default: issue_pv<D, 11>(d_o, a_p, vb, half_bytes, idesc_o, first); break;
-  }
-}
-
 // The MMA warp.  All 32 lanes run this loop with identical values (so the
 // descriptors stay warp-uniform) and one elected lane issues each MMA and
 // commit; every issue loop is fully unrolled.
-template <int D, bool kQTmem>
+template <int D, bool kQTmem, int NCH>
 __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32_t q_s, uint32_t k_s0,
                                            uint32_t v_s0, int nblk, const FwdParams& p) {
   volatile int* abort_flag = &bars.abort;
   const uint32_t kv_bytes = (uint32_t)p.Bk * D * 2;
   const uint32_t half_bytes = (uint32_t)p.Bk * 128;
-  const uint32_t idesc_s = ptx::idesc_bf16_f32(kQTile, (uint32_t)p.Bk, false);
+  const uint32_t idesc_s = ptx::idesc_bf16_f32(kQTile, (uint32_t)NCH * 16u, false);
   const uint32_t idesc_o = ptx::idesc_bf16_f32(kQTile, D, true);
-  const int nch = p.Bk / 16;
   bool ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(kQTmem ? &bars.q_tmem : &bars.q_full), 0,
                                                          abort_flag, p.err, kErrWaitMma, p.limit_ns));
   // Ring positions (stage, phase parity) advanced incrementally.
@@ -206,7 +189,7 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
       if (!ok) break;
       ptx::tc_fence_after_sync();
       const uint32_t kb = ks < p.kd ? k_s0 + ks * kv_bytes : q_s;
-      const uint32_t d_s = tmem + s_col(j & 1, p.Bk);
+      const uint32_t d_s = tmem + s_col(j & 1, NCH * 16);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t bdesc = ptx::smem_desc_sw128(kb + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024);
@@ -233,8 +216,8 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
                                                           kErrWaitMma, p.limit_ns));
       if (!ok) break;
       ptx::tc_fence_after_sync();
-      issue_pv_any<D>(nch, tmem + kColO, tmem + s_col(i & 1, p.Bk), v_s0 + vs * kv_bytes, half_bytes, idesc_o,
-                      i == 0);
+      issue_pv<D, NCH>(tmem + kColO, tmem + s_col(i & 1, NCH * 16), v_s0 + vs * kv_bytes, half_bytes, idesc_o,
+                       i == 0);
       ptx::mma_commit_elect(ptx::smem_addr(&bars.v_empty[vs]));
       ptx::mma_commit_elect(ptx::smem_addr(&bars.pv_done));
       if (i == nblk - 1) ptx::mma_commit_elect(ptx::smem_addr(&bars.o_full));
@@ -287,19 +270,6 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&r)[16], uint64_t sl2,
   }
 }
 
-// Issues the TMEM loads of chunks [c0, c0 + n) (n <= kHalfChunks).
-__device__ __forceinline__ void load_chunks(uint32_t sbase, int c0, int n, uint32_t (&r)[kHalfChunks][16]) {
-#pragma unroll
-  for (int u = 0; u < kHalfChunks; ++u)
-    if (u < n) ptx::tmem_ld16(sbase + (c0 + u) * 16, r[u]);
-}
-
-__device__ __forceinline__ void wait_chunks(int n, uint32_t (&r)[kHalfChunks][16]) {
-#pragma unroll
-  for (int u = 0; u < kHalfChunks; ++u)
-    if (u < n) ptx::tmem_ld_wait(r[u]);
-}
-
 // Row maximum of the block's raw scores (online path; one chunk at a time
 // to keep the fallback's registers low).
 __device__ __forceinline__ float block_max(uint32_t sbase, int nch) {
@@ -314,29 +284,35 @@ __device__ __forceinline__ float block_max(uint32_t sbase, int nch) {
   return mx;
 }
 
-// P for one S block, in two phases (halves of the block's chunks).  All TMEM
-// loads of a phase go out before any of its stores: a TMEM load issued after
-// a TMEM store of the same thread waits for that store, so loading chunk by
-// chunk between stores would pay that wait once per chunk; here it is paid
-// once per block.  Each chunk's bf16 P lands in the first 8 columns of the
-// chunk's own S columns (already read).
-__device__ __forceinline__ void block_softmax(uint32_t sbase, int nch, uint64_t sl2, uint64_t neg_m, float& l0,
-                                              float& l1, float& w0, float& w1) {
-  const int na = (nch + 1) / 2;
-  for (int c0 = 0; c0 < nch; c0 += na) {
-    const int n = min(na, nch - c0);
-    uint32_t r[kHalfChunks][16];
-    load_chunks(sbase, c0, n, r);
-    wait_chunks(n, r);
+// P for chunks [C0, C0 + N) of an S block.  All TMEM loads of the phase go
+// out before any of its stores: a TMEM load issued after a TMEM store of the
+// same thread waits for that store, so loading chunk by chunk between stores
+// would pay that wait once per chunk.  Each chunk's bf16 P lands in the first
+// 8 columns of the chunk's own S columns (already read).
+template <int C0, int N>
+__device__ __forceinline__ void softmax_phase(uint32_t sbase, uint64_t sl2, uint64_t neg_m, float& l0, float& l1,
+                                              float& w0, float& w1) {
+  uint32_t r[N][16];
 #pragma unroll
-    for (int u = 0; u < kHalfChunks; ++u)
-      if (u < n) {
-        if (u > 0) ptx::order_after(r[u], w1);
-        uint32_t pk[8];
-        exp_chunk(r[u], sl2, neg_m, l0, l1, w0, w1, pk);
-        ptx::tmem_st8(sbase + (c0 + u) * 16, pk);
-      }
+  for (int u = 0; u < N; ++u) ptx::tmem_ld16(sbase + (C0 + u) * 16, r[u]);
+#pragma unroll
+  for (int u = 0; u < N; ++u) ptx::tmem_ld_wait(r[u]);
+#pragma unroll
+  for (int u = 0; u < N; ++u) {
+    if (u > 0) ptx::order_after(r[u], w1);
+    uint32_t pk[8];
+    exp_chunk(r[u], sl2, neg_m, l0, l1, w0, w1, pk);
+    ptx::tmem_st8(sbase + (C0 + u) * 16, pk);
   }
+}
+
+// P for one S block of NCH chunks, in two phases (halves of the chunks).
+template <int NCH>
+__device__ __forceinline__ void block_softmax(uint32_t sbase, uint64_t sl2, uint64_t neg_m, float& l0, float& l1,
+                                              float& w0, float& w1) {
+  constexpr int kNa = (NCH + 1) / 2;
+  softmax_phase<0, kNa>(sbase, sl2, neg_m, l0, l1, w0, w1);
+  if constexpr (NCH > kNa) softmax_phase<kNa, NCH - kNa>(sbase, sl2, neg_m, l0, l1, w0, w1);
 }
 
 // Softmax and epilogue for one thread: row `trow` of the tile.
@@ -344,7 +320,7 @@ __device__ __forceinline__ void block_softmax(uint32_t sbase, int nch, uint64_t 
 // blocks of S buffer g, so the two groups ping-pong and neither talks to the
 // other until the epilogue.  Online heads: warpgroup 0 takes every block (the
 // running maximum is a serial chain); warpgroup 1 joins for the epilogue.
-template <int D, bool kQTmem>
+template <int D, bool kQTmem, int NCH>
 __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, uint32_t q_s, int warp, int lane,
                                                  int h, int f, int qt, int nblk, bool bounded,
                                                  const FwdParams& p) {
@@ -355,7 +331,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   const int row = qt * kQTile + trow;  // row inside the frame
   const bool valid = row < p.T;
   const int64_t grow = (int64_t)h * p.N + (int64_t)f * p.T + row;
-  const int nch = p.Bk / 16;
+  constexpr int nch = NCH;
   const uint64_t sl2 = ptx::f32x2(p.scale_log2, p.scale_log2);
   // Row maximum in log2 units of the scaled logits.
   float m_run = -INFINITY;
@@ -389,7 +365,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
     ok = __all_sync(0xffffffffu, got);
     if (!ok) break;
     ptx::tc_fence_after_sync();
-    const uint32_t sbase = tmem + lane_base + s_col(buf, p.Bk);
+    const uint32_t sbase = tmem + lane_base + s_col(buf, NCH * 16);
 
     if (!bounded) {
       const float mx = block_max(sbase, nch);
@@ -428,7 +404,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
       }
     }
 
-    block_softmax(sbase, nch, sl2, ptx::f32x2(-m_run, -m_run), l0, l1, w0, w1);
+    block_softmax<NCH>(sbase, sl2, ptx::f32x2(-m_run, -m_run), l0, l1, w0, w1);
     ptx::tmem_st_wait();
     ptx::tc_fence_before_sync();
     ptx::mbar_arrive(ptx::smem_addr(&bars.p_full[buf]));
@@ -472,10 +448,11 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   if (valid && g == 0) p.lse[grow] = (m_run + ptx::lg2(l)) * kLn2;
 }
 
-template <int D, bool kQTmem>
+template <int D, int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  constexpr bool kQTmem = q_fits_tmem(NCH * 16);
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
   const uint32_t tiles = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;  // 128B-swizzle atoms need 1 KB alignment
@@ -536,10 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ring_producer<D>(&tm_v, bars.v_full, bars.v_empty, p.vst, p.vst, v_s0, 0, nullptr, h, p.table[f], &bars.abort,
                        p);
   } else if (warp == kMmaWarp) {
-    mma_issuer<D, kQTmem>(bars, tmem, q_s, k_s0, v_s0, nblk, p);
+    mma_issuer<D, kQTmem, NCH>(bars, tmem, q_s, k_s0, v_s0, nblk, p);
   } else {
     const bool bounded = p.mode == FAS_MODE_BOUNDED || (p.mode == FAS_MODE_AUTO && p.elig[h] != 0);
-    softmax_epilogue<D, kQTmem>(bars, tmem, q_s, warp, lane, h, f, qt, nblk, bounded, p);
+    softmax_epilogue<D, kQTmem, NCH>(bars, tmem, q_s, warp, lane, h, f, qt, nblk, bounded, p);
   }
 
   ptx::tc_fence_before_sync();
@@ -567,11 +544,12 @@ __global__ void wait_selftest(unsigned int* err, uint64_t limit_ns) {
 
 constexpr size_t kSmemLimit = 232448;  // opt-in shared memory per block (sm_100 family)
 
-template <int D, bool kQTmem>
+template <int D, int NCH>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams p, int grid,
                      cudaStream_t st) {
   // Shared memory: [Q slot][kd K stages][vst V stages].  With Q in TMEM the
   // Q slot (sized for a K stage too) becomes K stage kd once Q is copied.
+  constexpr bool kQTmem = q_fits_tmem(NCH * 16);
   const size_t kv_bytes = (size_t)p.Bk * D * 2;
   const size_t q_bytes = (size_t)kQTile * D * 2;
   const size_t qslot = kQTmem ? (kv_bytes > q_bytes ? kv_bytes : q_bytes) : q_bytes;
@@ -588,22 +566,41 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   p.vst = vst;
   p.qslot_bytes = (uint32_t)qslot;
   const size_t smem = 1024 + qslot + (size_t)(kd + vst) * kv_bytes;
-  cudaError_t e = cudaFuncSetAttribute(attention_fwd<D, kQTmem>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attention_fwd<D, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  attention_fwd<D, kQTmem><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+  attention_fwd<D, NCH><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
+}
+
+// One instantiation per (head dimension, chunks per key block): the block
+// size is fixed per plan, so the kernel's loops are fully unrolled for it.
+template <int D>
+cudaError_t launch_dim(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                       int grid, cudaStream_t stream) {
+  static_assert(kMaxBlockK == 160, "extend the dispatch below");
+  if (p.Bk % 16 != 0) return cudaErrorInvalidValue;
+  switch (p.Bk / 16) {
+    case 1: return launch_d<D, 1>(tq, tk, tv, p, grid, stream);
+    case 2: return launch_d<D, 2>(tq, tk, tv, p, grid, stream);
+    case 3: return launch_d<D, 3>(tq, tk, tv, p, grid, stream);
+    case 4: return launch_d<D, 4>(tq, tk, tv, p, grid, stream);
+    case 5: return launch_d<D, 5>(tq, tk, tv, p, grid, stream);
+    case 6: return launch_d<D, 6>(tq, tk, tv, p, grid, stream);
+    case 7: return launch_d<D, 7>(tq, tk, tv, p, grid, stream);
+    case 8: return launch_d<D, 8>(tq, tk, tv, p, grid, stream);
+    case 9: return launch_d<D, 9>(tq, tk, tv, p, grid, stream);
+    case 10: return launch_d<D, 10>(tq, tk, tv, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_attention(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const FwdParams& p, int grid, cudaStream_t stream) {
-  const bool qt = q_fits_tmem(p.Bk);
-  if (d == 128) return qt ? launch_d<128, true>(tq, tk, tv, p, grid, stream)
-                          : launch_d<128, false>(tq, tk, tv, p, grid, stream);
-  if (d == 64) return qt ? launch_d<64, true>(tq, tk, tv, p, grid, stream)
-                         : launch_d<64, false>(tq, tk, tv, p, grid, stream);
+  if (d == 128) return launch_dim<128>(tq, tk, tv, p, grid, stream);
+  if (d == 64) return launch_dim<64>(tq, tk, tv, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 
