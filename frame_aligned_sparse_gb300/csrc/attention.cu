@@ -170,7 +170,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_o, uint32_t a_p, uint32_t vb
 // commit; every issue loop is fully unrolled.
 template <int D, bool kQTmem, int NCH>
 __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32_t q_s, uint32_t k_s0,
-                                           uint32_t v_s0, int nblk, const FwdParams& p) {
+                                           uint32_t v_s0, int nblk, bool bounded, const FwdParams& p) {
   volatile int* abort_flag = &bars.abort;
   const uint32_t kv_bytes = (uint32_t)p.Bk * D * 2;
   const uint32_t half_bytes = (uint32_t)p.Bk * 128;
@@ -184,10 +184,9 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
     if (j < nblk) {
       // S(j) = Q . K(j)^T : M=128, N=Bk, K=d; K is K-major with 128B swizzle;
       // Q comes from TMEM (bf16 pairs) or from shared memory like K.
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err,
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err,
                                                         kErrWaitMma, p.limit_ns));
       if (!ok) break;
-      ptx::tc_fence_after_sync();
       const uint32_t kb = ks < p.kd ? k_s0 + ks * kv_bytes : q_s;
       const uint32_t d_s = tmem + s_col(j & 1, NCH * 16);
 #pragma unroll
@@ -209,17 +208,18 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
     }
     if (j >= 1) {
       const int i = j - 1;
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag,
-                                                        p.err, kErrWaitMma, p.limit_ns));
-      if (ok)
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(&bars.v_full[vs]), vph, abort_flag, p.err,
-                                                          kErrWaitMma, p.limit_ns));
+      bool got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.v_full[vs]), vph, abort_flag, p.err, kErrWaitMma,
+                                       p.limit_ns);
+      if (got)
+        got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err,
+                                    kErrWaitMma, p.limit_ns);
+      ok = __all_sync(0xffffffffu, got);
       if (!ok) break;
       ptx::tc_fence_after_sync();
       issue_pv<D, NCH>(tmem + kColO, tmem + s_col(i & 1, NCH * 16), v_s0 + vs * kv_bytes, half_bytes, idesc_o,
                        i == 0);
       ptx::mma_commit_elect(ptx::smem_addr(&bars.v_empty[vs]));
-      ptx::mma_commit_elect(ptx::smem_addr(&bars.pv_done));
+      if (!bounded) ptx::mma_commit_elect(ptx::smem_addr(&bars.pv_done));
       if (i == nblk - 1) ptx::mma_commit_elect(ptx::smem_addr(&bars.o_full));
       if (++vs == p.vst) {
         vs = 0;
@@ -513,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ring_producer<D>(&tm_v, bars.v_full, bars.v_empty, p.vst, p.vst, v_s0, 0, nullptr, h, p.table[f], &bars.abort,
                        p);
   } else if (warp == kMmaWarp) {
-    mma_issuer<D, kQTmem, NCH>(bars, tmem, q_s, k_s0, v_s0, nblk, p);
+    const bool bounded = p.mode == FAS_MODE_BOUNDED || (p.mode == FAS_MODE_AUTO && p.elig[h] != 0);
+    mma_issuer<D, kQTmem, NCH>(bars, tmem, q_s, k_s0, v_s0, nblk, bounded, p);
   } else {
     const bool bounded = p.mode == FAS_MODE_BOUNDED || (p.mode == FAS_MODE_AUTO && p.elig[h] != 0);
     softmax_epilogue<D, kQTmem, NCH>(bars, tmem, q_s, warp, lane, h, f, qt, nblk, bounded, p);
