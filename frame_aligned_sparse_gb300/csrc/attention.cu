@@ -153,79 +153,104 @@ __device__ __forceinline__ void ring_producer(const CUtensorMap* tm, uint64_t* f
   }
 }
 
-// O += P(i) . V(i) as NCH fully unrolled 16-key MMAs: M=128, N=d, K=16 each;
-// P from TMEM (chunk kk's P sits in the first 8 columns of its own 16 S
-// columns), V MN-major in shared memory.
-template <int D, int NCH>
-__device__ __forceinline__ void issue_pv(uint32_t d_o, uint32_t a_p, uint32_t vb, uint32_t half_bytes,
-                                         uint32_t idesc_o, bool first) {
-#pragma unroll
-  for (int kk = 0; kk < NCH; ++kk)
-    ptx::mma_ts_elect(d_o, a_p + kk * 16, ptx::smem_desc_sw128(vb + kk * 2048, half_bytes, 1024), idesc_o,
-                      (!first || kk > 0) ? 1u : 0u);
-}
-
 // The MMA warp.  All 32 lanes run this loop with identical values (so the
-// descriptors stay warp-uniform) and one elected lane issues each MMA and
-// commit; every issue loop is fully unrolled.
+// waits and descriptors stay warp-uniform); one elected lane issues each
+// batch of MMAs and its commits as straight-line code.  The issuing warp
+// shares its scheduler with two softmax warps, and the tensor pipe's queue
+// is shallow, so every instruction between two MMAs can leave the pipe
+// idle: descriptors are therefore built once per CTA and advanced by adding
+// constants.  A tcgen05 shared-memory descriptor holds the start address
+// >> 4 in its low 14 bits and every tile here lies in the first 256 KB of
+// shared memory, so advancing the tile by b bytes adds b >> 4.
 template <int D, bool kQTmem, int NCH>
 __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32_t q_s, uint32_t k_s0,
                                            uint32_t v_s0, int nblk, bool bounded, const FwdParams& p) {
   volatile int* abort_flag = &bars.abort;
-  const uint32_t kv_bytes = (uint32_t)p.Bk * D * 2;
-  const uint32_t half_bytes = (uint32_t)p.Bk * 128;
-  const uint32_t idesc_s = ptx::idesc_bf16_f32(kQTile, (uint32_t)NCH * 16u, false);
-  const uint32_t idesc_o = ptx::idesc_bf16_f32(kQTile, D, true);
+  constexpr uint32_t kBk = NCH * 16;
+  constexpr uint32_t kKvBytes = kBk * D * 2;
+  constexpr uint32_t kHalfBytes = kBk * 128;  // one 64-column half of a K or V tile
+  constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kQTile, kBk, false);
+  constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kQTile, D, true);
+  // K (K-major, 128B swizzle): stage base; the stage in the Q slot; Q itself
+  // as an A operand; V (MN-major): stage base.
+  const uint64_t kdesc0 = ptx::smem_desc_sw128(k_s0, 16, 1024);
+  const uint64_t kdesc_qslot = ptx::smem_desc_sw128(q_s, 16, 1024);
+  const uint64_t qdesc = ptx::smem_desc_sw128(q_s, 16, 1024);
+  const uint64_t vdesc0 = ptx::smem_desc_sw128(v_s0, kHalfBytes, 1024);
   bool ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(kQTmem ? &bars.q_tmem : &bars.q_full), 0,
                                                          abort_flag, p.err, kErrWaitMma, p.limit_ns));
   // Ring positions (stage, phase parity) advanced incrementally.
   int ks = 0, kph = 0, vs = 0, vph = 0;
-  for (int j = 0; ok && j <= nblk; ++j) {
-    if (j < nblk) {
-      // S(j) = Q . K(j)^T : M=128, N=Bk, K=d; K is K-major with 128B swizzle;
-      // Q comes from TMEM (bf16 pairs) or from shared memory like K.
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err,
-                                                        kErrWaitMma, p.limit_ns));
-      if (!ok) break;
-      const uint32_t kb = ks < p.kd ? k_s0 + ks * kv_bytes : q_s;
-      const uint32_t d_s = tmem + s_col(j & 1, NCH * 16);
+  // S(j) = Q . K(j)^T : M=128, N=Bk, K=d in d/16 MMAs (elected lane only).
+  auto issue_s = [&](int j) {
+    const uint64_t kdesc = ks < p.kd ? kdesc0 + (uint64_t)(ks * (kKvBytes >> 4)) : kdesc_qslot;
+    const uint32_t d_s = tmem + s_col(j & 1, kBk);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t bdesc = ptx::smem_desc_sw128(kb + (kk >> 2) * half_bytes + (kk & 3) * 32, 16, 1024);
-        if (kQTmem) {
-          ptx::mma_ts_elect(d_s, tmem + kColQ + kk * 8, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-        } else {
-          const uint32_t a = q_s + (kk >> 2) * (kQTile * 128) + (kk & 3) * 32;
-          ptx::mma_ss_elect(d_s, ptx::smem_desc_sw128(a, 16, 1024), bdesc, idesc_s, kk > 0 ? 1u : 0u);
-        }
-      }
-      ptx::mma_commit_elect(ptx::smem_addr(&bars.s_full[j & 1]));
-      ptx::mma_commit_elect(ptx::smem_addr(&bars.k_empty[ks]));
-      if (++ks == p.kst) {
-        ks = 0;
-        kph ^= 1;
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint64_t bdesc = kdesc + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+      if (kQTmem) {
+        ptx::mma_ts(d_s, tmem + kColQ + kk * 8, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+      } else {
+        const uint64_t adesc = qdesc + (((kk >> 2) * (kQTile * 128) + (kk & 3) * 32) >> 4);
+        ptx::mma_ss(d_s, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
       }
     }
-    if (j >= 1) {
-      const int i = j - 1;
-      bool got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.v_full[vs]), vph, abort_flag, p.err, kErrWaitMma,
-                                       p.limit_ns);
-      if (got)
-        got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err,
-                                    kErrWaitMma, p.limit_ns);
-      ok = __all_sync(0xffffffffu, got);
-      if (!ok) break;
-      ptx::tc_fence_after_sync();
-      issue_pv<D, NCH>(tmem + kColO, tmem + s_col(i & 1, NCH * 16), v_s0 + vs * kv_bytes, half_bytes, idesc_o,
-                       i == 0);
-      ptx::mma_commit_elect(ptx::smem_addr(&bars.v_empty[vs]));
-      if (!bounded) ptx::mma_commit_elect(ptx::smem_addr(&bars.pv_done));
-      if (i == nblk - 1) ptx::mma_commit_elect(ptx::smem_addr(&bars.o_full));
-      if (++vs == p.vst) {
-        vs = 0;
-        vph ^= 1;
-      }
+    ptx::mma_commit(ptx::smem_addr(&bars.s_full[j & 1]));
+    ptx::mma_commit(ptx::smem_addr(&bars.k_empty[ks]));
+  };
+  auto next_k = [&]() {
+    if (++ks == p.kst) {
+      ks = 0;
+      kph ^= 1;
     }
+  };
+  // The first two S blocks fill both S buffers.
+  for (int j = 0; ok && j < 2 && j < nblk; ++j) {
+    ok = __all_sync(0xffffffffu, ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err,
+                                                      kErrWaitMma, p.limit_ns));
+    if (!ok) break;
+    if (ptx::elect_one()) issue_s(j);
+    __syncwarp();
+    next_k();
+  }
+  // Then one batch per block i: O += P(i) . V(i), followed by S(i+2) into the
+  // S buffer that P(i) occupied (the pipe runs them in order, so P(i) is read
+  // before it is overwritten).  One wait point per batch, for V(i), P(i) and
+  // K(i+2) together: each wait between MMAs leaves the pipe idle, because
+  // an MMA is accepted only about one instruction ahead of its execution.
+  for (int i = 0; ok && i < nblk; ++i) {
+    const bool more = i + 2 < nblk;
+    bool got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.v_full[vs]), vph, abort_flag, p.err, kErrWaitMma,
+                                     p.limit_ns);
+    if (got)
+      got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err,
+                                  kErrWaitMma, p.limit_ns);
+    if (got && more)
+      got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err, kErrWaitMma,
+                                  p.limit_ns);
+    ok = __all_sync(0xffffffffu, got);
+    if (!ok) break;
+    ptx::tc_fence_after_sync();
+    // P(i) . V(i): M=128, N=d, one K=16 MMA per 16-key chunk; P from TMEM
+    // (chunk kk's bf16 P sits in the first 8 columns of its own 16 S
+    // columns), V MN-major in shared memory.
+    const uint64_t vdesc = vdesc0 + (uint64_t)(vs * (kKvBytes >> 4));
+    const uint32_t a_p = tmem + s_col(i & 1, kBk);
+    if (ptx::elect_one()) {
+#pragma unroll
+      for (int kk = 0; kk < NCH; ++kk)
+        ptx::mma_ts(tmem + kColO, a_p + kk * 16, vdesc + ((kk * 2048) >> 4), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+      ptx::mma_commit(ptx::smem_addr(&bars.v_empty[vs]));
+      if (!bounded) ptx::mma_commit(ptx::smem_addr(&bars.pv_done));
+      if (i == nblk - 1) ptx::mma_commit(ptx::smem_addr(&bars.o_full));
+      if (more) issue_s(i + 2);
+    }
+    __syncwarp();
+    if (++vs == p.vst) {
+      vs = 0;
+      vph ^= 1;
+    }
+    if (more) next_k();
   }
   // Every MMA issued above completes before TMEM is released.
   ptx::mma_commit_elect(ptx::smem_addr(&bars.drain));
@@ -255,6 +280,20 @@ __device__ __forceinline__ void stage_q_row(uint32_t q_s, uint32_t taddr, int tr
   }
 }
 
+// Of the 8 element pairs of a 16-column chunk, this many take 2^x on the FMA
+// pipe (ptx::ex2_poly_x2) and the rest on the special-function unit.  At
+// d = 128 one exponential per (query, key) pair on the SFU alone takes as
+// long as the pair's share of both MMAs, so moving part of them to the FMA
+// pipe is what lets the tensor pipe, not the SFU, set the pace.
+#ifndef FAS_EX2_POLY_PAIRS
+#define FAS_EX2_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairs = FAS_EX2_POLY_PAIRS;
+static_assert(kPolyPairs >= 0 && kPolyPairs <= 8, "pairs per 16-column chunk");
+
+// Spreads the kPolyPairs software pairs evenly over the chunk.
+__host__ __device__ constexpr bool poly_pair(int e) { return ((e + 1) * kPolyPairs) / 8 != (e * kPolyPairs) / 8; }
+
 // Softmax of one 16-column chunk held in registers: P = 2^(S*sl2 - m) (two
 // lanes per packed instruction), both row sums, P packed to bf16 pairs.
 __device__ __forceinline__ void exp_chunk(const uint32_t (&r)[16], uint64_t sl2, uint64_t neg_m, float& l0,
@@ -263,7 +302,13 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&r)[16], uint64_t sl2,
   for (int e = 0; e < 8; ++e) {
     float x0, x1;
     ptx::fma_f32x2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), sl2, neg_m);
-    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+    float p0, p1;
+    if (poly_pair(e)) {
+      ptx::ex2_poly_x2(p0, p1, x0, x1);
+    } else {
+      p0 = ptx::ex2(x0);
+      p1 = ptx::ex2(x1);
+    }
     ptx::add_f32x2(l0, l1, p0, p1);
     pk[e] = ptx::pack_bf16x2(p0, p1);
     ptx::add_f32x2(w0, w1, __uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u));
@@ -289,19 +334,36 @@ __device__ __forceinline__ float block_max(uint32_t sbase, int nch) {
 // same thread waits for that store, so loading chunk by chunk between stores
 // would pay that wait once per chunk.  Each chunk's bf16 P lands in the first
 // 8 columns of the chunk's own S columns (already read).
+#ifndef FAS_SM_ACC4
+#define FAS_SM_ACC4 0
+#endif
 template <int C0, int N>
 __device__ __forceinline__ void softmax_phase(uint32_t sbase, uint64_t sl2, uint64_t neg_m, float& l0, float& l1,
-                                              float& w0, float& w1) {
+                                              float& w0, float& w1, float& l2, float& l3, float& w2, float& w3) {
   uint32_t r[N][16];
 #pragma unroll
   for (int u = 0; u < N; ++u) ptx::tmem_ld16(sbase + (C0 + u) * 16, r[u]);
 #pragma unroll
   for (int u = 0; u < N; ++u) ptx::tmem_ld_wait(r[u]);
+#ifndef FAS_SM_ORDER
+#define FAS_SM_ORDER 1
+#endif
+  uint32_t prev = 0;
 #pragma unroll
   for (int u = 0; u < N; ++u) {
+#if FAS_SM_ORDER == 1
     if (u > 0) ptx::order_after(r[u], w1);
+#elif FAS_SM_ORDER == 2
+    if (u > 0) ptx::order_after(r[u], __uint_as_float(prev));
+#endif
     uint32_t pk[8];
+#if FAS_SM_ACC4
+    if (u & 1) exp_chunk(r[u], sl2, neg_m, l2, l3, w2, w3, pk);
+    else exp_chunk(r[u], sl2, neg_m, l0, l1, w0, w1, pk);
+#else
     exp_chunk(r[u], sl2, neg_m, l0, l1, w0, w1, pk);
+#endif
+    prev = pk[1];
     ptx::tmem_st8(sbase + (C0 + u) * 16, pk);
   }
 }
@@ -309,10 +371,10 @@ __device__ __forceinline__ void softmax_phase(uint32_t sbase, uint64_t sl2, uint
 // P for one S block of NCH chunks, in two phases (halves of the chunks).
 template <int NCH>
 __device__ __forceinline__ void block_softmax(uint32_t sbase, uint64_t sl2, uint64_t neg_m, float& l0, float& l1,
-                                              float& w0, float& w1) {
+                                              float& w0, float& w1, float& l2, float& l3, float& w2, float& w3) {
   constexpr int kNa = (NCH + 1) / 2;
-  softmax_phase<0, kNa>(sbase, sl2, neg_m, l0, l1, w0, w1);
-  if constexpr (NCH > kNa) softmax_phase<kNa, NCH - kNa>(sbase, sl2, neg_m, l0, l1, w0, w1);
+  softmax_phase<0, kNa>(sbase, sl2, neg_m, l0, l1, w0, w1, l2, l3, w2, w3);
+  if constexpr (NCH > kNa) softmax_phase<kNa, NCH - kNa>(sbase, sl2, neg_m, l0, l1, w0, w1, l2, l3, w2, w3);
 }
 
 // Softmax and epilogue for one thread: row `trow` of the tile.
@@ -341,6 +403,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   // MMA actually uses (for normalising O, so the output is a convex
   // combination of V rows even when the largest probability is not 1).
   float l0 = 0.f, l1 = 0.f, w0 = 0.f, w1 = 0.f;
+  float l2 = 0.f, l3 = 0.f, w2 = 0.f, w3 = 0.f;
   bool ok = true;
 
   if (kQTmem && g == 0) {
@@ -382,6 +445,10 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
           l1 *= alpha;
           w0 *= alpha;
           w1 *= alpha;
+          l2 *= alpha;
+          l3 *= alpha;
+          w2 *= alpha;
+          w3 *= alpha;
         }
         if (__any_sync(0xffffffffu, need)) {
           // The accumulator may be rescaled only once P(j-1).V(j-1) is done.
@@ -404,7 +471,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
       }
     }
 
-    block_softmax<NCH>(sbase, sl2, ptx::f32x2(-m_run, -m_run), l0, l1, w0, w1);
+    block_softmax<NCH>(sbase, sl2, ptx::f32x2(-m_run, -m_run), l0, l1, w0, w1, l2, l3, w2, w3);
     ptx::tmem_st_wait();
     ptx::tc_fence_before_sync();
     ptx::mbar_arrive(ptx::smem_addr(&bars.p_full[buf]));
@@ -416,8 +483,8 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
     const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.o_full), 0, abort_flag, p.err, kErrWaitSoftmax, p.limit_ns);
     ok = __all_sync(0xffffffffu, got);
   }
-  bars.red[g][0][trow] = l0 + l1;
-  bars.red[g][1][trow] = w0 + w1;
+  bars.red[g][0][trow] = (l0 + l1) + (l2 + l3);
+  bars.red[g][1][trow] = (w0 + w1) + (w2 + w3);
   ptx::named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
   float l = 0.f, lw = 0.f;
 #pragma unroll

@@ -211,6 +211,17 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// True in exactly one lane of the (fully active) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -324,6 +335,45 @@ __device__ __forceinline__ void order_after(uint32_t (&r)[16], float after) {
                  "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
                  "+r"(r[15])
                : "f"(after));
+}
+
+// 2^x for two lanes on the FMA and integer pipes instead of the
+// special-function unit.  Cody-Waite style range reduction: x = n + f with
+// n = rint(x) and f in [-1/2, 1/2]; 2^f is a cubic fitted to minimise the
+// largest relative error on that interval (iterated re-weighted least
+// squares, max relative error 7.5e-5, well under a bf16 half-ulp of 2^-9);
+// the result's exponent field is then raised by n with one integer add.
+// Adding 1.5 * 2^23 rounds x to an integer held in the low mantissa bits of
+// the sum, and those bits shifted left by 23 are exactly n << 23 (mod 2^32).
+// Inputs are clamped at -125 so that the result stays a normal number (the
+// exponent field cannot wrap); callers only pass x <= 16.
+__device__ __forceinline__ void ex2_poly_x2(float& y0, float& y1, float x0, float x1) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  constexpr float kC0 = 0.99992806f, kC1 = 0.69326097f, kC2 = 0.24261114f, kC3 = 0.055171672f;
+  x0 = fmaxf(x0, -125.0f);
+  x1 = fmaxf(x1, -125.0f);
+  uint32_t t0, t1, p0, p1;
+  asm("{\n\t.reg .b64 x, t, j, f, p, rr, nr, m1, c0, c1, c2, c3;\n\t"
+      "mov.b64 x, {%4, %5};\n\t"
+      "mov.b64 rr, {%6, %6};\n\t"
+      "mov.b64 nr, {%7, %7};\n\t"
+      "mov.b64 m1, {%8, %8};\n\t"
+      "mov.b64 c0, {%9, %9};\n\t"
+      "mov.b64 c1, {%10, %10};\n\t"
+      "mov.b64 c2, {%11, %11};\n\t"
+      "mov.b64 c3, {%12, %12};\n\t"
+      "add.rn.f32x2 t, x, rr;\n\t"
+      "add.rn.f32x2 j, t, nr;\n\t"
+      "fma.rn.f32x2 f, j, m1, x;\n\t"
+      "fma.rn.f32x2 p, f, c3, c2;\n\t"
+      "fma.rn.f32x2 p, p, f, c1;\n\t"
+      "fma.rn.f32x2 p, p, f, c0;\n\t"
+      "mov.b64 {%0, %1}, t;\n\t"
+      "mov.b64 {%2, %3}, p;\n\t}"
+      : "=r"(t0), "=r"(t1), "=r"(p0), "=r"(p1)
+      : "f"(x0), "f"(x1), "f"(kRound), "f"(-kRound), "f"(-1.0f), "f"(kC0), "f"(kC1), "f"(kC2), "f"(kC3));
+  y0 = __uint_as_float(p0 + (t0 << 23));
+  y1 = __uint_as_float(p1 + (t1 << 23));
 }
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
