@@ -153,15 +153,18 @@ __device__ __forceinline__ void ring_producer(const CUtensorMap* tm, uint64_t* f
   }
 }
 
-// The MMA warp.  All 32 lanes run this loop with identical values (so the
-// waits and descriptors stay warp-uniform); one elected lane issues each
-// batch of MMAs and its commits as straight-line code.  The issuing warp
-// shares its scheduler with two softmax warps, and the tensor pipe's queue
-// is shallow, so every instruction between two MMAs can leave the pipe
-// idle: descriptors are therefore built once per CTA and advanced by adding
-// constants.  A tcgen05 shared-memory descriptor holds the start address
-// >> 4 in its low 14 bits and every tile here lies in the first 256 KB of
-// shared memory, so advancing the tile by b bytes adds b >> 4.
+// The MMA issuer: one elected lane of the MMA warp runs the whole loop,
+// waits included, while the other lanes wait at the warp's reconvergence.
+// An MMA is accepted several instructions ahead of its execution only while
+// the issuing thread runs undisturbed: a whole warp that votes on each wait
+// and reconverges around an elected lane per batch measured tens of clocks
+// of pipe idle per batch.  The region is entered through elect.sync (not a
+// lane-index test) so that its arithmetic stays warp-uniform; a lane-index
+// branch here measured 30% slower.  Shared-memory descriptors are built once
+// per CTA and advanced by constant adds: a tcgen05 shared-memory descriptor
+// holds the start address >> 4 in its low 14 bits and every tile here lies
+// in the first 256 KB of shared memory, so advancing a tile by b bytes adds
+// b >> 4.
 template <int D, bool kQTmem, int NCH>
 __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32_t q_s, uint32_t k_s0,
                                            uint32_t v_s0, int nblk, bool bounded, const FwdParams& p) {
@@ -177,11 +180,11 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
   const uint64_t kdesc_qslot = ptx::smem_desc_sw128(q_s, 16, 1024);
   const uint64_t qdesc = ptx::smem_desc_sw128(q_s, 16, 1024);
   const uint64_t vdesc0 = ptx::smem_desc_sw128(v_s0, kHalfBytes, 1024);
-  bool ok = __all_sync(0xffffffffu, ptx::mbar_wait<true>(ptx::smem_addr(kQTmem ? &bars.q_tmem : &bars.q_full), 0,
-                                                         abort_flag, p.err, kErrWaitMma, p.limit_ns));
+  bool ok = ptx::mbar_wait<true>(ptx::smem_addr(kQTmem ? &bars.q_tmem : &bars.q_full), 0, abort_flag, p.err,
+                                 kErrWaitMma, p.limit_ns);
   // Ring positions (stage, phase parity) advanced incrementally.
   int ks = 0, kph = 0, vs = 0, vph = 0;
-  // S(j) = Q . K(j)^T : M=128, N=Bk, K=d in d/16 MMAs (elected lane only).
+  // S(j) = Q . K(j)^T : M=128, N=Bk, K=d in d/16 MMAs.
   auto issue_s = [&](int j) {
     const uint64_t kdesc = ks < p.kd ? kdesc0 + (uint64_t)(ks * (kKvBytes >> 4)) : kdesc_qslot;
     const uint32_t d_s = tmem + s_col(j & 1, kBk);
@@ -197,8 +200,6 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
     }
     ptx::mma_commit(ptx::smem_addr(&bars.s_full[j & 1]));
     ptx::mma_commit(ptx::smem_addr(&bars.k_empty[ks]));
-  };
-  auto next_k = [&]() {
     if (++ks == p.kst) {
       ks = 0;
       kph ^= 1;
@@ -206,29 +207,20 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
   };
   // The first two S blocks fill both S buffers.
   for (int j = 0; ok && j < 2 && j < nblk; ++j) {
-    ok = __all_sync(0xffffffffu, ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err,
-                                                      kErrWaitMma, p.limit_ns));
-    if (!ok) break;
-    if (ptx::elect_one()) issue_s(j);
-    __syncwarp();
-    next_k();
+    ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err, kErrWaitMma, p.limit_ns);
+    if (ok) issue_s(j);
   }
   // Then one batch per block i: O += P(i) . V(i), followed by S(i+2) into the
   // S buffer that P(i) occupied (the pipe runs them in order, so P(i) is read
-  // before it is overwritten).  One wait point per batch, for V(i), P(i) and
-  // K(i+2) together: each wait between MMAs leaves the pipe idle, because
-  // an MMA is accepted only about one instruction ahead of its execution.
+  // before it is overwritten), after one wait point for V(i), P(i) and K(i+2).
   for (int i = 0; ok && i < nblk; ++i) {
     const bool more = i + 2 < nblk;
-    bool got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.v_full[vs]), vph, abort_flag, p.err, kErrWaitMma,
-                                     p.limit_ns);
-    if (got)
-      got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err,
-                                  kErrWaitMma, p.limit_ns);
-    if (got && more)
-      got = ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err, kErrWaitMma,
-                                  p.limit_ns);
-    ok = __all_sync(0xffffffffu, got);
+    ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.v_full[vs]), vph, abort_flag, p.err, kErrWaitMma, p.limit_ns);
+    if (ok)
+      ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err, kErrWaitMma,
+                                 p.limit_ns);
+    if (ok && more)
+      ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err, kErrWaitMma, p.limit_ns);
     if (!ok) break;
     ptx::tc_fence_after_sync();
     // P(i) . V(i): M=128, N=d, one K=16 MMA per 16-key chunk; P from TMEM
@@ -236,24 +228,20 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
     // columns), V MN-major in shared memory.
     const uint64_t vdesc = vdesc0 + (uint64_t)(vs * (kKvBytes >> 4));
     const uint32_t a_p = tmem + s_col(i & 1, kBk);
-    if (ptx::elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < NCH; ++kk)
-        ptx::mma_ts(tmem + kColO, a_p + kk * 16, vdesc + ((kk * 2048) >> 4), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-      ptx::mma_commit(ptx::smem_addr(&bars.v_empty[vs]));
-      if (!bounded) ptx::mma_commit(ptx::smem_addr(&bars.pv_done));
-      if (i == nblk - 1) ptx::mma_commit(ptx::smem_addr(&bars.o_full));
-      if (more) issue_s(i + 2);
-    }
-    __syncwarp();
+    for (int kk = 0; kk < NCH; ++kk)
+      ptx::mma_ts(tmem + kColO, a_p + kk * 16, vdesc + ((kk * 2048) >> 4), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+    ptx::mma_commit(ptx::smem_addr(&bars.v_empty[vs]));
+    if (!bounded) ptx::mma_commit(ptx::smem_addr(&bars.pv_done));
+    if (i == nblk - 1) ptx::mma_commit(ptx::smem_addr(&bars.o_full));
     if (++vs == p.vst) {
       vs = 0;
       vph ^= 1;
     }
-    if (more) next_k();
+    if (more) issue_s(i + 2);
   }
   // Every MMA issued above completes before TMEM is released.
-  ptx::mma_commit_elect(ptx::smem_addr(&bars.drain));
+  ptx::mma_commit(ptx::smem_addr(&bars.drain));
   drain_wait(ptx::smem_addr(&bars.drain), 0, p.err, p.limit_ns);
 }
 
@@ -581,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        p);
   } else if (warp == kMmaWarp) {
     const bool bounded = p.mode == FAS_MODE_BOUNDED || (p.mode == FAS_MODE_AUTO && p.elig[h] != 0);
-    mma_issuer<D, kQTmem, NCH>(bars, tmem, q_s, k_s0, v_s0, nblk, bounded, p);
+    if (ptx::elect_one()) mma_issuer<D, kQTmem, NCH>(bars, tmem, q_s, k_s0, v_s0, nblk, bounded, p);
+    __syncwarp();
   } else {
     const bool bounded = p.mode == FAS_MODE_BOUNDED || (p.mode == FAS_MODE_AUTO && p.elig[h] != 0);
     softmax_epilogue<D, kQTmem, NCH>(bars, tmem, q_s, warp, lane, h, f, qt, nblk, bounded, p);
