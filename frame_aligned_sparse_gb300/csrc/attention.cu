@@ -77,7 +77,8 @@ struct Barriers {
   uint64_t v_full[kMaxStages];
   uint64_t v_empty[kMaxStages];
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t pa_full[2];  // P of the first (NCH + 1) / 2 chunks of the block in S buffer b
+  uint64_t p_full[2];   // P of the remaining chunks
   uint64_t pv_done;
   uint64_t o_full;
   uint64_t drain;
@@ -174,6 +175,7 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
   constexpr uint32_t kHalfBytes = kBk * 128;  // one 64-column half of a K or V tile
   constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kQTile, kBk, false);
   constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kQTile, D, true);
+  constexpr int kPa = (NCH + 1) / 2;  // chunks of P released first
   // K (K-major, 128B swizzle): stage base; the stage in the Q slot; Q itself
   // as an A operand; V (MN-major): stage base.
   const uint64_t kdesc0 = ptx::smem_desc_sw128(k_s0, 16, 1024);
@@ -215,22 +217,31 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
   // before it is overwritten), after one wait point for V(i), P(i) and K(i+2).
   for (int i = 0; ok && i < nblk; ++i) {
     const bool more = i + 2 < nblk;
+    // P(i) . V(i): M=128, N=d, one K=16 MMA per 16-key chunk; P from TMEM
+    // (chunk kk's bf16 P sits in the first 8 columns of its own 16 S
+    // columns), V MN-major in shared memory.  The first kPa chunks go as
+    // soon as their P is released; the rest, and S(i+2), after the rest of
+    // P(i) and K(i+2).
+    const uint64_t vdesc = vdesc0 + (uint64_t)(vs * (kKvBytes >> 4));
+    const uint32_t a_p = tmem + s_col(i & 1, kBk);
     ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.v_full[vs]), vph, abort_flag, p.err, kErrWaitMma, p.limit_ns);
     if (ok)
-      ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err, kErrWaitMma,
+      ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.pa_full[i & 1]), (i >> 1) & 1, abort_flag, p.err, kErrWaitMma,
                                  p.limit_ns);
+    if (!ok) break;
+    ptx::tc_fence_after_sync();
+#pragma unroll
+    for (int kk = 0; kk < kPa; ++kk)
+      ptx::mma_ts(tmem + kColO, a_p + kk * 16, vdesc + ((kk * 2048) >> 4), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+    ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.p_full[i & 1]), (i >> 1) & 1, abort_flag, p.err, kErrWaitMma,
+                               p.limit_ns);
     if (ok && more)
       ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.k_full[ks]), kph, abort_flag, p.err, kErrWaitMma, p.limit_ns);
     if (!ok) break;
     ptx::tc_fence_after_sync();
-    // P(i) . V(i): M=128, N=d, one K=16 MMA per 16-key chunk; P from TMEM
-    // (chunk kk's bf16 P sits in the first 8 columns of its own 16 S
-    // columns), V MN-major in shared memory.
-    const uint64_t vdesc = vdesc0 + (uint64_t)(vs * (kKvBytes >> 4));
-    const uint32_t a_p = tmem + s_col(i & 1, kBk);
 #pragma unroll
-    for (int kk = 0; kk < NCH; ++kk)
-      ptx::mma_ts(tmem + kColO, a_p + kk * 16, vdesc + ((kk * 2048) >> 4), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+    for (int kk = kPa; kk < NCH; ++kk)
+      ptx::mma_ts(tmem + kColO, a_p + kk * 16, vdesc + ((kk * 2048) >> 4), idesc_o, 1u);
     ptx::mma_commit(ptx::smem_addr(&bars.v_empty[vs]));
     if (!bounded) ptx::mma_commit(ptx::smem_addr(&bars.pv_done));
     if (i == nblk - 1) ptx::mma_commit(ptx::smem_addr(&bars.o_full));
@@ -322,47 +333,23 @@ __device__ __forceinline__ float block_max(uint32_t sbase, int nch) {
 // same thread waits for that store, so loading chunk by chunk between stores
 // would pay that wait once per chunk.  Each chunk's bf16 P lands in the first
 // 8 columns of the chunk's own S columns (already read).
-#ifndef FAS_SM_ACC4
-#define FAS_SM_ACC4 0
-#endif
 template <int C0, int N>
 __device__ __forceinline__ void softmax_phase(uint32_t sbase, uint64_t sl2, uint64_t neg_m, float& l0, float& l1,
-                                              float& w0, float& w1, float& l2, float& l3, float& w2, float& w3) {
-  uint32_t r[N][16];
+                                              float& w0, float& w1) {
+  if constexpr (N > 0) {
+    uint32_t r[N][16];
 #pragma unroll
-  for (int u = 0; u < N; ++u) ptx::tmem_ld16(sbase + (C0 + u) * 16, r[u]);
+    for (int u = 0; u < N; ++u) ptx::tmem_ld16(sbase + (C0 + u) * 16, r[u]);
 #pragma unroll
-  for (int u = 0; u < N; ++u) ptx::tmem_ld_wait(r[u]);
-#ifndef FAS_SM_ORDER
-#define FAS_SM_ORDER 1
-#endif
-  uint32_t prev = 0;
+    for (int u = 0; u < N; ++u) ptx::tmem_ld_wait(r[u]);
 #pragma unroll
-  for (int u = 0; u < N; ++u) {
-#if FAS_SM_ORDER == 1
-    if (u > 0) ptx::order_after(r[u], w1);
-#elif FAS_SM_ORDER == 2
-    if (u > 0) ptx::order_after(r[u], __uint_as_float(prev));
-#endif
-    uint32_t pk[8];
-#if FAS_SM_ACC4
-    if (u & 1) exp_chunk(r[u], sl2, neg_m, l2, l3, w2, w3, pk);
-    else exp_chunk(r[u], sl2, neg_m, l0, l1, w0, w1, pk);
-#else
-    exp_chunk(r[u], sl2, neg_m, l0, l1, w0, w1, pk);
-#endif
-    prev = pk[1];
-    ptx::tmem_st8(sbase + (C0 + u) * 16, pk);
+    for (int u = 0; u < N; ++u) {
+      if (u > 0) ptx::order_after(r[u], w1);
+      uint32_t pk[8];
+      exp_chunk(r[u], sl2, neg_m, l0, l1, w0, w1, pk);
+      ptx::tmem_st8(sbase + (C0 + u) * 16, pk);
+    }
   }
-}
-
-// P for one S block of NCH chunks, in two phases (halves of the chunks).
-template <int NCH>
-__device__ __forceinline__ void block_softmax(uint32_t sbase, uint64_t sl2, uint64_t neg_m, float& l0, float& l1,
-                                              float& w0, float& w1, float& l2, float& l3, float& w2, float& w3) {
-  constexpr int kNa = (NCH + 1) / 2;
-  softmax_phase<0, kNa>(sbase, sl2, neg_m, l0, l1, w0, w1, l2, l3, w2, w3);
-  if constexpr (NCH > kNa) softmax_phase<kNa, NCH - kNa>(sbase, sl2, neg_m, l0, l1, w0, w1, l2, l3, w2, w3);
 }
 
 // Softmax and epilogue for one thread: row `trow` of the tile.
@@ -382,6 +369,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   const bool valid = row < p.T;
   const int64_t grow = (int64_t)h * p.N + (int64_t)f * p.T + row;
   constexpr int nch = NCH;
+  constexpr int kPa = (NCH + 1) / 2;  // chunks in the first half of a block
   const uint64_t sl2 = ptx::f32x2(p.scale_log2, p.scale_log2);
   // Row maximum in log2 units of the scaled logits.
   float m_run = -INFINITY;
@@ -391,7 +379,6 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   // MMA actually uses (for normalising O, so the output is a convex
   // combination of V rows even when the largest probability is not 1).
   float l0 = 0.f, l1 = 0.f, w0 = 0.f, w1 = 0.f;
-  float l2 = 0.f, l3 = 0.f, w2 = 0.f, w3 = 0.f;
   bool ok = true;
 
   if (kQTmem && g == 0) {
@@ -433,10 +420,6 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
           l1 *= alpha;
           w0 *= alpha;
           w1 *= alpha;
-          l2 *= alpha;
-          l3 *= alpha;
-          w2 *= alpha;
-          w3 *= alpha;
         }
         if (__any_sync(0xffffffffu, need)) {
           // The accumulator may be rescaled only once P(j-1).V(j-1) is done.
@@ -459,7 +442,14 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
       }
     }
 
-    block_softmax<NCH>(sbase, sl2, ptx::f32x2(-m_run, -m_run), l0, l1, w0, w1, l2, l3, w2, w3);
+    // P of the block's first chunks is released as soon as it is stored, so
+    // that their P.V MMAs run while the rest of the block is exponentiated.
+    const uint64_t neg_m = ptx::f32x2(-m_run, -m_run);
+    softmax_phase<0, kPa>(sbase, sl2, neg_m, l0, l1, w0, w1);
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before_sync();
+    ptx::mbar_arrive(ptx::smem_addr(&bars.pa_full[buf]));
+    softmax_phase<kPa, NCH - kPa>(sbase, sl2, neg_m, l0, l1, w0, w1);
     ptx::tmem_st_wait();
     ptx::tc_fence_before_sync();
     ptx::mbar_arrive(ptx::smem_addr(&bars.p_full[buf]));
@@ -471,8 +461,8 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
     const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.o_full), 0, abort_flag, p.err, kErrWaitSoftmax, p.limit_ns);
     ok = __all_sync(0xffffffffu, got);
   }
-  bars.red[g][0][trow] = (l0 + l1) + (l2 + l3);
-  bars.red[g][1][trow] = (w0 + w1) + (w2 + w3);
+  bars.red[g][0][trow] = l0 + l1;
+  bars.red[g][1][trow] = w0 + w1;
   ptx::named_barrier_sync(kSoftmaxBarrier, kSoftmaxThreads);
   float l = 0.f, lw = 0.f;
 #pragma unroll
@@ -534,7 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_addr(&bars.s_full[b]), 1);
-      ptx::mbar_init(ptx::smem_addr(&bars.p_full[b]), 32 * 4);  // one warpgroup per block
+      ptx::mbar_init(ptx::smem_addr(&bars.pa_full[b]), 32 * 4);  // one warpgroup per block
+      ptx::mbar_init(ptx::smem_addr(&bars.p_full[b]), 32 * 4);
     }
     ptx::mbar_init(ptx::smem_addr(&bars.pv_done), 1);
     ptx::mbar_init(ptx::smem_addr(&bars.o_full), 1);
