@@ -313,18 +313,18 @@ def run_fas(args, w):
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
     prepass_ms = ms_step - fwd_avg
 
-    # End to end through the public API: pinned host inputs in, host results out.
+    # End to end through the public API: pinned host inputs in, host results
+    # out (fas_forward_host), every copy inside the timed region.
     pin = {t: host[t].pin_memory() for t in "qkv"}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     e2e_steps = max(1, min(args.steps, 10))
 
     def e2e_step():
-        for t, dst in (("q", q), ("k", k), ("v", v)):
-            dst.copy_(pin[t], non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        # The host-buffer call: per head group, copy-in, prepass + attention
+        # and copy-out run on the library's streams, overlapped across groups.
+        plan()
+        fas.fas_forward_host(pin["q"], pin["k"], pin["v"], out_h, lse_h, mode=args.mode, stream=stream)
 
     e2e_step()
     torch.cuda.synchronize(dev)

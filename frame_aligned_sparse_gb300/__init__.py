@@ -24,7 +24,7 @@ __all__ = [
     "FasError", "PlanInfo", "MODES", "library_path", "load",
     "fas_plan", "fas_plan_describe", "fas_prepass", "fas_forward", "fas_free",
     "fas_status", "fas_prepass_readback", "fas_selftest_wait_timeout", "fas_last_launch_count",
-    "fas_prepass_noalloc",
+    "fas_prepass_noalloc", "fas_forward_host",
 ]
 
 FAS_OK, FAS_ERR_ARG, FAS_ERR_STATE, FAS_ERR_ALIGN, FAS_ERR_CUDA, FAS_ERR_TIMEOUT, FAS_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
@@ -79,6 +79,7 @@ _SIGS = {
                                                               ctypes.c_void_p]),
     "fas_prepass": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "fas_forward": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_void_p]),
+    "fas_forward_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "fas_free": (ctypes.c_int, []),
     "fas_status": (ctypes.c_int, [ctypes.c_void_p]),
     "fas_prepass_readback": (ctypes.c_int, [ctypes.c_void_p] * 6),
@@ -203,6 +204,40 @@ def fas_forward(q, k, v, out=None, lse=None, mode: str = "auto", stream=None):
     rc = load().fas_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                             MODES[mode], _stream_handle(stream))
     _check("fas_forward", rc)
+    return out, lse
+
+
+def _check_host_tensor(name, t, shape, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, the plan needs {tuple(shape)}")
+
+
+def fas_forward_host(q, k, v, out=None, lse=None, mode: str = "auto", heads_per_group: int = 0, stream=None):
+    """Prepass + attention on HOST tensors (bf16 [H, N, d]; page-locked for
+    copy/compute overlap), pipelined over head groups on the library's own
+    streams; see ``fas_forward_host`` in fas.h.  Returns (out, lse) host
+    tensors, complete once ``stream`` (default: the current CUDA stream) has
+    reached this point."""
+    import torch
+    shape = _qkv_shape()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_host_tensor(name, t, shape, torch.bfloat16)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, pin_memory=True)
+    if lse is None:
+        lse = torch.empty(shape[:2], dtype=torch.float32, pin_memory=True)
+    _check_host_tensor("out", out, shape, torch.bfloat16)
+    _check_host_tensor("lse", lse, shape[:2], torch.float32)
+    rc = load().fas_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                 MODES[mode], int(heads_per_group), _stream_handle(stream))
+    _check("fas_forward_host", rc)
     return out, lse
 
 

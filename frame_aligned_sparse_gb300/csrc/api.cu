@@ -41,10 +41,27 @@ struct State {
   const void* pre_k = nullptr;
   int last_launches = 0;
   fas_plan_info info{};
+  // fas_forward_host: library-owned device copies of q, k, v, out, lse, the
+  // work list regrouped by head group, and the pipeline's streams/events.
+  void* io = nullptr;
+  uint16_t *dq = nullptr, *dk = nullptr, *dv = nullptr, *dout = nullptr;
+  float* dlse = nullptr;
+  CUtensorMap io_tq{}, io_tk{}, io_tv{};
+  int4* gwork = nullptr;
+  int gwork_hg = 0;                  // heads per group the regrouped list was built for
+  std::vector<int> gwork_off;        // first item of each group (plus the end)
+  cudaStream_t st_h2d = nullptr, st_comp = nullptr, st_d2h = nullptr;
+  std::vector<cudaEvent_t> ev_in, ev_done;
+  cudaEvent_t ev_entry = nullptr, ev_exit = nullptr;
+  bool exit_recorded = false;
 };
 
 State g_state;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// Default heads per group of fas_forward_host: small enough that the first
+// group's copy-in and the last group's copy-out are short, large enough
+// that each group's attention launch fills the GPU many times over.
+constexpr int kHostGroupHeads = 4;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -60,12 +77,23 @@ void fill_info(const HostPlan& p, fas_plan_info* info) {
 }
 
 void release() {
-  if (g_state.arena) {
+  State& s = g_state;
+  if (s.arena || s.io || s.st_h2d) {
     int cur = -1;
     cudaGetDevice(&cur);
-    if (g_state.device >= 0 && cur != g_state.device) cudaSetDevice(g_state.device);
-    cudaFree(g_state.arena);
-    if (cur >= 0 && cur != g_state.device) cudaSetDevice(cur);
+    if (s.device >= 0 && cur != s.device) cudaSetDevice(s.device);
+    for (cudaStream_t st : {s.st_h2d, s.st_comp, s.st_d2h})
+      if (st) cudaStreamSynchronize(st);
+    for (cudaStream_t st : {s.st_h2d, s.st_comp, s.st_d2h})
+      if (st) cudaStreamDestroy(st);
+    for (auto* evs : {&s.ev_in, &s.ev_done})
+      for (cudaEvent_t e : *evs) cudaEventDestroy(e);
+    for (cudaEvent_t e : {s.ev_entry, s.ev_exit})
+      if (e) cudaEventDestroy(e);
+    if (s.gwork) cudaFree(s.gwork);
+    if (s.io) cudaFree(s.io);
+    if (s.arena) cudaFree(s.arena);
+    if (cur >= 0 && cur != s.device) cudaSetDevice(cur);
   }
   g_state = State();
 }
@@ -134,6 +162,135 @@ int encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
   return r == CUDA_SUCCESS ? FAS_OK : FAS_ERR_CUDA;
 }
 
+// Prepass arguments for heads [h0, h0 + nh) of q and k (head-major layouts:
+// every per-head buffer is offset by h0).
+fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
+  const HostPlan& p = g_state.plan;
+  State& s = g_state;
+  const size_t H0 = (size_t)h0, Nf = p.Nf, D = p.d, C = p.chunks, N = (size_t)p.N;
+  fas::PrepassArgs a;
+  a.q = static_cast<const uint16_t*>(q) + H0 * N * D;
+  a.k = static_cast<const uint16_t*>(k) + H0 * N * D;
+  a.table = s.table;
+  a.partial = s.partial + H0 * Nf * C * D;
+  a.mu = s.mu + H0 * D;
+  a.fsum = s.fsum + H0 * Nf * D;
+  a.mpart = s.mpart + H0 * Nf * C;
+  a.frame_max = s.frame_max + H0 * Nf;
+  a.mvis = s.mvis + H0 * Nf;
+  a.kbarc = s.kbarc + H0 * Nf * D;
+  a.row_bound = s.row_bound + H0 * N;
+  a.gpart = s.gpart + H0 * Nf * C;
+  a.stat = s.stat + H0;
+  a.elig = s.elig + H0;
+  a.N = p.N;
+  a.T = p.T;
+  a.Nf = p.Nf;
+  a.H = nh;
+  a.d = p.d;
+  a.chunks = p.chunks;
+  a.scale = (float)(1.0 / sqrt((double)p.d));
+  return a;
+}
+
+// Tensor maps of q, k, v (device bf16 [H, N, d]).  Q is [H][Nf][T][d] so a
+// tile's rows past the frame end read as zeros.
+int encode_qkv(const void* q, const void* k, const void* v, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
+  const HostPlan& p = g_state.plan;
+  const cuuint64_t D = (cuuint64_t)p.d;
+  {
+    const cuuint64_t dims[4] = {D, (cuuint64_t)p.T, (cuuint64_t)p.Nf, (cuuint64_t)p.H};
+    const cuuint64_t strides[3] = {D * 2, (cuuint64_t)p.T * D * 2, (cuuint64_t)p.N * D * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)fas::kQTile, 1, 1};
+    if (encode(tq, q, 4, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {D, (cuuint64_t)p.N, (cuuint64_t)p.H};
+  const cuuint64_t strides[2] = {D * 2, (cuuint64_t)p.N * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)p.Bk, 1};
+  if (encode(tk, k, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
+  if (encode(tv, v, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
+  return FAS_OK;
+}
+
+// Launches the attention kernel over work items [first, first + count).
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const int4* work,
+                       int count, void* out, float* lse, int mode, cudaStream_t st) {
+  const HostPlan& p = g_state.plan;
+  State& s = g_state;
+  fas::FwdParams fp;
+  fp.work = work;
+  fp.table = s.table;
+  fp.row_bound = s.row_bound;
+  fp.elig = s.elig;
+  fp.out = static_cast<uint16_t*>(out);
+  fp.lse = lse;
+  fp.err = s.err;
+  fp.N = p.N;
+  fp.T = p.T;
+  fp.Bk = p.Bk;
+  fp.mode = mode;
+  fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.d));
+  fp.limit_ns = fas::kWaitLimitNs;
+  return fas::launch_attention(p.d, tq, tk, tv, fp, count, st);
+}
+
+// fas_forward_host resources: device copies of the inputs and outputs, the
+// work list regrouped by head group (heaviest items first inside a group),
+// three streams and the per-group events.  Built on first use per plan.
+int ensure_host_pipeline(int hg) {
+  State& s = g_state;
+  const HostPlan& p = s.plan;
+  const size_t hnd = (size_t)p.H * (size_t)p.N * (size_t)p.d;
+  if (!s.io) {
+    const size_t bytes = 4 * hnd * 2 + (size_t)p.H * (size_t)p.N * 4;
+    if (cudaMalloc(&s.io, bytes) != cudaSuccess) {
+      s.io = nullptr;
+      return FAS_ERR_CUDA;
+    }
+    uint16_t* b = static_cast<uint16_t*>(s.io);
+    s.dq = b;
+    s.dk = b + hnd;
+    s.dv = b + 2 * hnd;
+    s.dout = b + 3 * hnd;
+    s.dlse = reinterpret_cast<float*>(b + 4 * hnd);
+    if (encode_qkv(s.dq, s.dk, s.dv, &s.io_tq, &s.io_tk, &s.io_tv) != FAS_OK) return FAS_ERR_CUDA;
+  }
+  if (!s.st_h2d) {
+    for (cudaStream_t* st : {&s.st_h2d, &s.st_comp, &s.st_d2h})
+      if (cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) != cudaSuccess) return FAS_ERR_CUDA;
+    for (cudaEvent_t* e : {&s.ev_entry, &s.ev_exit})
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
+  }
+  const int groups = (p.H + hg - 1) / hg;
+  while ((int)s.ev_in.size() < groups) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
+    s.ev_in.push_back(a);
+    if (cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
+    s.ev_done.push_back(b);
+  }
+  if (s.gwork_hg != hg) {
+    // The plan's list is heaviest first over all heads; keeping that order
+    // inside each group keeps every group's launch heaviest first.
+    std::vector<int32_t> grouped;
+    grouped.reserve(p.work.size());
+    s.gwork_off.assign(1, 0);
+    for (int g = 0; g < groups; ++g) {
+      for (size_t i = 0; i < p.work.size(); i += 4)
+        if (p.work[i] / hg == g) grouped.insert(grouped.end(), p.work.begin() + i, p.work.begin() + i + 4);
+      s.gwork_off.push_back((int)(grouped.size() / 4));
+    }
+    if (!s.gwork && cudaMalloc(&s.gwork, p.work.size() * 4) != cudaSuccess) {
+      s.gwork = nullptr;
+      return FAS_ERR_CUDA;
+    }
+    if (cudaMemcpy(s.gwork, grouped.data(), grouped.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+      return FAS_ERR_CUDA;
+    s.gwork_hg = hg;
+  }
+  return FAS_OK;
+}
+
 int check_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FAS_ERR_CUDA;
@@ -198,28 +355,7 @@ int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_h
   const HostPlan& p = g_state.plan;
   State& s = g_state;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  fas::PrepassArgs a;
-  a.q = q;
-  a.k = k;
-  a.table = s.table;
-  a.partial = s.partial;
-  a.mu = s.mu;
-  a.fsum = s.fsum;
-  a.mpart = s.mpart;
-  a.frame_max = s.frame_max;
-  a.mvis = s.mvis;
-  a.kbarc = s.kbarc;
-  a.row_bound = s.row_bound;
-  a.gpart = s.gpart;
-  a.stat = s.stat;
-  a.elig = s.elig;
-  a.N = p.N;
-  a.T = p.T;
-  a.Nf = p.Nf;
-  a.H = p.H;
-  a.d = p.d;
-  a.chunks = p.chunks;
-  a.scale = (float)(1.0 / sqrt((double)p.d));
+  const fas::PrepassArgs a = prepass_args(q, k, 0, p.H);
   const int n = fas::launch_prepass(a, st);
   s.last_launches = n > 0 ? n : 0;
   if (n < 0) return FAS_ERR_CUDA;
@@ -247,39 +383,76 @@ int fas_forward(const void* q, const void* k, const void* v, void* out, float* l
   if (rc != FAS_OK) return rc;
   const HostPlan& p = g_state.plan;
   State& s = g_state;
-  const cuuint64_t D = (cuuint64_t)p.d;
-  // Q: [H][Nf][T][d] so a tile's rows past the frame end read as zeros.
   CUtensorMap tq, tk, tv;
-  {
-    const cuuint64_t dims[4] = {D, (cuuint64_t)p.T, (cuuint64_t)p.Nf, (cuuint64_t)p.H};
-    const cuuint64_t strides[3] = {D * 2, (cuuint64_t)p.T * D * 2, (cuuint64_t)p.N * D * 2};
-    const cuuint32_t box[4] = {64, (cuuint32_t)fas::kQTile, 1, 1};
-    if (encode(&tq, q, 4, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
-  }
-  {
-    const cuuint64_t dims[3] = {D, (cuuint64_t)p.N, (cuuint64_t)p.H};
-    const cuuint64_t strides[2] = {D * 2, (cuuint64_t)p.N * D * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)p.Bk, 1};
-    if (encode(&tk, k, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
-    if (encode(&tv, v, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
-  }
-  fas::FwdParams fp;
-  fp.work = s.work;
-  fp.table = s.table;
-  fp.row_bound = s.row_bound;
-  fp.elig = s.elig;
-  fp.out = static_cast<uint16_t*>(out);
-  fp.lse = lse;
-  fp.err = s.err;
-  fp.N = p.N;
-  fp.T = p.T;
-  fp.Bk = p.Bk;
-  fp.mode = mode;
-  fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.d));
-  fp.limit_ns = fas::kWaitLimitNs;
-  const cudaError_t e = fas::launch_attention(p.d, tq, tk, tv, fp, p.n_work, static_cast<cudaStream_t>(cuda_stream));
+  if (encode_qkv(q, k, v, &tq, &tk, &tv) != FAS_OK) return FAS_ERR_CUDA;
+  const cudaError_t e = launch_fwd(tq, tk, tv, s.work, p.n_work, out, lse, mode, static_cast<cudaStream_t>(cuda_stream));
   s.last_launches = e == cudaSuccess ? 1 : 0;
   return e == cudaSuccess ? FAS_OK : FAS_ERR_CUDA;
+}
+
+int fas_forward_host(const void* q, const void* k, const void* v, void* out, float* lse, int mode,
+                     int heads_per_group, void* cuda_stream) {
+  if (!g_state.planned) return FAS_ERR_STATE;
+  if (!q || !k || !v || !out || !lse) return FAS_ERR_ARG;
+  if (mode != FAS_MODE_AUTO && mode != FAS_MODE_ONLINE && mode != FAS_MODE_BOUNDED) return FAS_ERR_ARG;
+  const HostPlan& p = g_state.plan;
+  if (heads_per_group < 0 || heads_per_group > p.H) return FAS_ERR_ARG;
+  const int hg = heads_per_group > 0 ? heads_per_group : (p.H < kHostGroupHeads ? p.H : kHostGroupHeads);
+  int rc = check_device();
+  if (rc != FAS_OK) return rc;
+  rc = ensure_encoder();
+  if (rc != FAS_OK) return rc;
+  rc = ensure_host_pipeline(hg);
+  if (rc != FAS_OK) return rc;
+  State& s = g_state;
+  cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
+  const size_t head_elems = (size_t)p.N * (size_t)p.d;
+  const int groups = (p.H + hg - 1) / hg;
+  int launches = 0;
+  // Start after the caller's earlier work, and after the previous call of
+  // this function has finished with the library's device copies.
+  if (cudaEventRecord(s.ev_entry, caller) != cudaSuccess) return FAS_ERR_CUDA;
+  for (cudaStream_t st : {s.st_h2d, s.st_comp, s.st_d2h}) {
+    if (cudaStreamWaitEvent(st, s.ev_entry, 0) != cudaSuccess) return FAS_ERR_CUDA;
+    if (s.exit_recorded && cudaStreamWaitEvent(st, s.ev_exit, 0) != cudaSuccess) return FAS_ERR_CUDA;
+  }
+  for (int g = 0; g < groups; ++g) {
+    const int h0 = g * hg, nh = (p.H - h0 < hg) ? p.H - h0 : hg;
+    const size_t off = (size_t)h0 * head_elems, n = (size_t)nh * head_elems;
+    // In: q, k, v of the group's heads (contiguous slices of [H, N, d]).
+    const void* src[3] = {q, k, v};
+    uint16_t* dst[3] = {s.dq, s.dk, s.dv};
+    for (int t = 0; t < 3; ++t)
+      if (cudaMemcpyAsync(dst[t] + off, static_cast<const uint16_t*>(src[t]) + off, n * 2, cudaMemcpyHostToDevice,
+                          s.st_h2d) != cudaSuccess)
+        return FAS_ERR_CUDA;
+    if (cudaEventRecord(s.ev_in[g], s.st_h2d) != cudaSuccess) return FAS_ERR_CUDA;
+    // Compute: prepass and attention for the group's heads.
+    if (cudaStreamWaitEvent(s.st_comp, s.ev_in[g], 0) != cudaSuccess) return FAS_ERR_CUDA;
+    const int np = fas::launch_prepass(prepass_args(s.dq, s.dk, h0, nh), s.st_comp);
+    if (np < 0) return FAS_ERR_CUDA;
+    launches += np;
+    const int i0 = s.gwork_off[g], ni = s.gwork_off[g + 1] - i0;
+    if (launch_fwd(s.io_tq, s.io_tk, s.io_tv, s.gwork + i0, ni, s.dout, s.dlse, mode, s.st_comp) != cudaSuccess)
+      return FAS_ERR_CUDA;
+    ++launches;
+    if (cudaEventRecord(s.ev_done[g], s.st_comp) != cudaSuccess) return FAS_ERR_CUDA;
+    // Out: the group's rows of out and lse.
+    if (cudaStreamWaitEvent(s.st_d2h, s.ev_done[g], 0) != cudaSuccess) return FAS_ERR_CUDA;
+    if (cudaMemcpyAsync(static_cast<uint16_t*>(out) + off, s.dout + off, n * 2, cudaMemcpyDeviceToHost, s.st_d2h) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(lse + (size_t)h0 * p.N, s.dlse + (size_t)h0 * p.N, (size_t)nh * p.N * 4,
+                        cudaMemcpyDeviceToHost, s.st_d2h) != cudaSuccess)
+      return FAS_ERR_CUDA;
+  }
+  // The caller's stream continues once every group's results are on the host.
+  if (cudaEventRecord(s.ev_exit, s.st_d2h) != cudaSuccess) return FAS_ERR_CUDA;
+  s.exit_recorded = true;
+  if (cudaStreamWaitEvent(caller, s.ev_exit, 0) != cudaSuccess) return FAS_ERR_CUDA;
+  s.pre_q = s.dq;
+  s.pre_k = s.dk;
+  s.last_launches = launches;
+  return FAS_OK;
 }
 
 int fas_free(void) {

@@ -132,6 +132,28 @@ int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_h
 int fas_forward(const void* q, const void* k, const void* v, void* out, float* lse,
                 int mode, void* cuda_stream);
 
+/* Attention with inputs and outputs in HOST memory: the call a process makes
+ * when its activations live on the host.  q, k, v, out: host bf16 [H, N, d];
+ * lse: host fp32 [H, N]; layouts and results as for fas_prepass followed by
+ * fas_forward (bit-identical outputs).  The heads are independent, so the
+ * call splits them into groups of heads_per_group (0 = library default, 4)
+ * and pipelines the groups on three library-owned streams: while group g
+ * is computed (prepass and attention), group g+1 is copied in and group g-1
+ * copied out.  The host buffers should be page-locked (cudaHostAlloc or
+ * cudaHostRegister); pageable buffers give correct results without the
+ * overlap.  On first use per plan the library allocates device copies of
+ * q, k, v, out and lse (4*H*N*d*2 + 4*H*N bytes, released by fas_free or
+ * the next fas_plan), creates its streams and events, and regroups the work
+ * list.  The work starts after everything already enqueued on cuda_stream
+ * and the call returns at once: out and lse are complete when cuda_stream
+ * reaches this point (synchronise it, or call fas_status, before reading
+ * them).  Consecutive calls are ordered with each other.  Needs a plan;
+ * heads_per_group outside 0..H returns FAS_ERR_ARG; no pointer alignment is
+ * required.  Afterwards fas_prepass_readback reports this call's
+ * statistics. */
+int fas_forward_host(const void* q, const void* k, const void* v, void* out, float* lse,
+                     int mode, int heads_per_group, void* cuda_stream);
+
 /* Release every library-owned device buffer and forget the plan. */
 int fas_free(void);
 

@@ -224,3 +224,60 @@ def test_argument_and_order_errors():
     assert lib.fas_forward(c.q.data_ptr(), c.k.data_ptr(), c.v.data_ptr(), out.data_ptr(), lse.data_ptr(), 7,
                            st) == fas.FAS_ERR_ARG
     assert fas.fas_status() == fas.FAS_OK
+
+
+def host_bf16(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+
+@pytest.mark.parametrize("name,groups", [("tiny", [0, 1, 2]), ("mid", [0, 1, 5, 16])])
+def test_forward_host_matches_device_path(name, groups):
+    """fas_forward_host (host buffers, head groups pipelined over copy and
+    compute streams) runs the same kernels per head as fas_prepass +
+    fas_forward, so its outputs must be bit-identical, for any group size,
+    and within tolerance of the oracle."""
+    c = case(name)
+    hq, hk, hv = (host_bf16(c.x[t]) for t in "qkv")
+    for mode in ("auto", "online"):
+        _, out_d, lse_d = c.run(mode)
+        out_d, lse_d = out_d.cpu(), lse_d.cpu()
+        for hg in groups:
+            out_h, lse_h = fas.fas_forward_host(hq, hk, hv, mode=mode, heads_per_group=hg)
+            torch.cuda.current_stream().synchronize()
+            assert fas.fas_status() == fas.FAS_OK
+            assert torch.equal(out_h.view(torch.int16), out_d.view(torch.int16)), (name, mode, hg)
+            assert torch.equal(lse_h.view(torch.int32), lse_d.view(torch.int32)), (name, mode, hg)
+        c.check(out_h, lse_h, f"{name}/{mode}/host")
+
+
+def test_forward_host_720p_sampled_rows():
+    """The host-buffer path on the full 720p SR chunk, as the benchmark's
+    end-to-end measurement runs it (default head groups), against the
+    oracle on sampled rows; eligibility read back afterwards."""
+    c = case("720p")
+    c.plan()
+    hq, hk, hv = (host_bf16(c.x[t]) for t in "qkv")
+    out_h, lse_h = fas.fas_forward_host(hq, hk, hv, mode="auto")
+    torch.cuda.current_stream().synchronize()
+    assert fas.fas_status() == fas.FAS_OK
+    c.check(out_h, lse_h, "720p/host")
+    want = np.ones(c.w.heads, dtype=bool)
+    want[c.x["modified_heads"]] = False
+    assert np.array_equal(fas.fas_prepass_readback()["elig"].astype(bool), want)
+
+
+def test_forward_host_argument_errors():
+    c = case("tiny")
+    c.plan()
+    lib = fas.load()
+    st = torch.cuda.current_stream().cuda_stream
+    hq = host_bf16(c.x["q"])
+    out = torch.empty(hq.shape, dtype=torch.bfloat16, pin_memory=True)
+    lse = torch.empty(c.w.heads, c.w.tokens, dtype=torch.float32, pin_memory=True)
+    p = [hq.data_ptr()] * 3 + [out.data_ptr(), lse.data_ptr()]
+    assert lib.fas_forward_host(*p, 0, c.w.heads + 1, st) == fas.FAS_ERR_ARG
+    assert lib.fas_forward_host(*p, 0, -1, st) == fas.FAS_ERR_ARG
+    assert lib.fas_forward_host(*p, 9, 0, st) == fas.FAS_ERR_ARG
+    assert lib.fas_forward_host(None, *p[1:], 0, 0, st) == fas.FAS_ERR_ARG
+    with pytest.raises(TypeError):
+        fas.fas_forward_host(c.q, c.k, c.v)  # device tensors are refused

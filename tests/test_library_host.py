@@ -126,6 +126,7 @@ def test_calls_out_of_order_return_state_error():
     lib.fas_free()
     assert lib.fas_prepass(None, None, None, None) == fas.FAS_ERR_STATE
     assert lib.fas_forward(None, None, None, None, None, 0, None) == fas.FAS_ERR_STATE
+    assert lib.fas_forward_host(None, None, None, None, None, 0, 0, None) == fas.FAS_ERR_STATE
     assert lib.fas_status(None) == fas.FAS_ERR_STATE
     assert lib.fas_prepass_readback(None, None, None, None, None, None) == fas.FAS_ERR_STATE
     assert lib.fas_selftest_wait_timeout(0, None) == fas.FAS_ERR_ARG
