@@ -249,6 +249,8 @@ def run_fas(args, w):
 
     x = workloads.generate(w)
     host = {t: torch.from_numpy(x[t].view(np.int16)).view(torch.bfloat16) for t in "qkv"}
+    if args.layout == "nhd":
+        host = {t: a.transpose(0, 1).contiguous() for t, a in host.items()}
     q, k, v = (host[t].to(dev) for t in "qkv")
     H, N, d = w.heads, w.tokens, w.head_dim
     out = torch.empty_like(q)
@@ -261,6 +263,7 @@ def run_fas(args, w):
 
     info = plan()
     assert abs(info.visible_flops - flops) < 1.0
+    fas.fas_set_layout(args.layout)
 
     launches = [0]
 
@@ -359,7 +362,8 @@ def run_fas(args, w):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, 720p-like SR chunk)",
         "config": {
-            "workload": w.describe(), "mode": args.mode, "block_k": info.block_k, "q_tile": info.q_tile,
+            "workload": w.describe(), "mode": args.mode, "layout": args.layout, "block_k": info.block_k,
+            "q_tile": info.q_tile,
             "work_items": info.n_work, "visible_tflop_per_step": flops / 1e12,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": l2_note(3 * H * N * d * 2),
@@ -396,6 +400,8 @@ def main():
     ap.add_argument("--workload", default="720p", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--mode", default="auto", choices=["auto", "online", "bounded"])
     ap.add_argument("--block-k", type=int, default=0)
+    ap.add_argument("--layout", default="hnd", choices=["hnd", "nhd"],
+                    help="q, k, v, out as [H, N, d] or token-major [N, H, d]")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

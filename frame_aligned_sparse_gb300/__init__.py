@@ -24,13 +24,14 @@ __all__ = [
     "FasError", "PlanInfo", "MODES", "library_path", "load",
     "fas_plan", "fas_plan_describe", "fas_prepass", "fas_forward", "fas_free",
     "fas_status", "fas_prepass_readback", "fas_selftest_wait_timeout", "fas_last_launch_count",
-    "fas_prepass_noalloc", "fas_forward_host",
+    "fas_prepass_noalloc", "fas_forward_host", "fas_set_layout", "LAYOUTS",
 ]
 
 FAS_OK, FAS_ERR_ARG, FAS_ERR_STATE, FAS_ERR_ALIGN, FAS_ERR_CUDA, FAS_ERR_TIMEOUT, FAS_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 FAS_ERR_SCRATCH = -7
 FAS_NOALLOC_SCRATCH_BYTES = 4 << 20
 MODES = {"auto": 0, "online": 1, "bounded": 2}
+LAYOUTS = {"hnd": 0, "nhd": 1}  # q, k, v, out as [H, N, d] or [N, H, d]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -88,6 +89,7 @@ _SIGS = {
     "fas_prepass_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 6 +
                             [ctypes.c_void_p] * 4),
     "fas_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fas_set_layout": (ctypes.c_int, [ctypes.c_int]),
 }
 
 
@@ -139,8 +141,18 @@ def fas_plan(frame_tokens: int, n_frames: int, ref_frames: int, window_radius: i
                             ctypes.byref(c))
     _check("fas_plan", rc)
     info = _info(c)
-    _PLAN.update(heads=heads, head_dim=head_dim, tokens=info.tokens, info=info)
+    geometry = (frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, info.block_k)
+    if _PLAN.get("geometry") != geometry:
+        _PLAN["layout"] = "hnd"  # a new plan starts head-major (the library resets it too)
+    _PLAN.update(heads=heads, head_dim=head_dim, tokens=info.tokens, info=info, geometry=geometry)
     return info
+
+
+def fas_set_layout(layout: str) -> None:
+    """Layout of q, k, v and out for the following calls: "hnd" ([H, N, d])
+    or "nhd" ([N, H, d]); lse stays [H, N].  See ``fas_set_layout`` in fas.h."""
+    _check("fas_set_layout", load().fas_set_layout(LAYOUTS[layout]))
+    _PLAN["layout"] = layout
 
 
 def fas_plan_describe(frame_tokens: int, n_frames: int, ref_frames: int, window_radius: int, heads: int,
@@ -171,9 +183,16 @@ def _check_tensor(name, t, shape, dtype):
 
 
 def _qkv_shape():
+    """Shape of q, k, v and out in the current layout."""
     if not _PLAN:
         raise FasError("fas_plan", FAS_ERR_STATE, "no plan")
+    if _PLAN.get("layout", "hnd") == "nhd":
+        return (_PLAN["tokens"], _PLAN["heads"], _PLAN["head_dim"])
     return (_PLAN["heads"], _PLAN["tokens"], _PLAN["head_dim"])
+
+
+def _lse_shape():
+    return (_PLAN["heads"], _PLAN["tokens"])
 
 
 def fas_prepass(q, k, stream=None, want_elig: bool = False) -> Optional[np.ndarray]:
@@ -182,7 +201,7 @@ def fas_prepass(q, k, stream=None, want_elig: bool = False) -> Optional[np.ndarr
     shape = _qkv_shape()
     _check_tensor("q", q, shape, torch.bfloat16)
     _check_tensor("k", k, shape, torch.bfloat16)
-    elig = np.zeros(shape[0], dtype=np.uint8) if want_elig else None
+    elig = np.zeros(_PLAN["heads"], dtype=np.uint8) if want_elig else None
     rc = load().fas_prepass(q.data_ptr(), k.data_ptr(), _stream_handle(stream),
                             elig.ctypes.data if want_elig else None)
     _check("fas_prepass", rc)
@@ -198,9 +217,9 @@ def fas_forward(q, k, v, out=None, lse=None, mode: str = "auto", stream=None):
     if out is None:
         out = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
     if lse is None:
-        lse = torch.empty(shape[:2], dtype=torch.float32, device=q.device)
+        lse = torch.empty(_lse_shape(), dtype=torch.float32, device=q.device)
     _check_tensor("out", out, shape, torch.bfloat16)
-    _check_tensor("lse", lse, shape[:2], torch.float32)
+    _check_tensor("lse", lse, _lse_shape(), torch.float32)
     rc = load().fas_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                             MODES[mode], _stream_handle(stream))
     _check("fas_forward", rc)
@@ -232,9 +251,9 @@ def fas_forward_host(q, k, v, out=None, lse=None, mode: str = "auto", heads_per_
     if out is None:
         out = torch.empty(shape, dtype=torch.bfloat16, pin_memory=True)
     if lse is None:
-        lse = torch.empty(shape[:2], dtype=torch.float32, pin_memory=True)
+        lse = torch.empty(_lse_shape(), dtype=torch.float32, pin_memory=True)
     _check_host_tensor("out", out, shape, torch.bfloat16)
-    _check_host_tensor("lse", lse, shape[:2], torch.float32)
+    _check_host_tensor("lse", lse, _lse_shape(), torch.float32)
     rc = load().fas_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                  MODES[mode], int(heads_per_group), _stream_handle(stream))
     _check("fas_forward_host", rc)
@@ -255,7 +274,7 @@ def fas_status(stream=None) -> int:
 
 
 def fas_prepass_readback(stream=None, row_bound: bool = False) -> dict:
-    H, N, d = _qkv_shape()
+    H, N, d = _PLAN["heads"], _PLAN["tokens"], _PLAN["head_dim"]
     nf = _PLAN["info"].total_frames
     res = {"mu": np.zeros((H, d), np.float32), "frame_max": np.zeros((H, nf), np.float32),
            "stat": np.zeros(H, np.float32), "elig": np.zeros(H, np.uint8)}

@@ -40,6 +40,7 @@ struct State {
   const void* pre_q = nullptr;
   const void* pre_k = nullptr;
   int last_launches = 0;
+  int layout = FAS_LAYOUT_HND;  // of q, k, v and out
   fas_plan_info info{};
   // fas_forward_host: library-owned device copies of q, k, v, out, lse, the
   // work list regrouped by head group, and the pipeline's streams/events.
@@ -162,15 +163,28 @@ int encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
   return r == CUDA_SUCCESS ? FAS_OK : FAS_ERR_CUDA;
 }
 
-// Prepass arguments for heads [h0, h0 + nh) of q and k (head-major layouts:
-// every per-head buffer is offset by h0).
+// Element strides of q, k, v and out in the current layout: between two
+// tokens of one head, and between two heads.
+int64_t row_stride() {
+  const HostPlan& p = g_state.plan;
+  return g_state.layout == FAS_LAYOUT_NHD ? (int64_t)p.H * p.d : (int64_t)p.d;
+}
+int64_t head_stride() {
+  const HostPlan& p = g_state.plan;
+  return g_state.layout == FAS_LAYOUT_NHD ? (int64_t)p.d : p.N * (int64_t)p.d;
+}
+
+// Prepass arguments for heads [h0, h0 + nh) of q and k (every per-head
+// statistics buffer is head-major, so it is offset by h0).
 fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   const HostPlan& p = g_state.plan;
   State& s = g_state;
   const size_t H0 = (size_t)h0, Nf = p.Nf, D = p.d, C = p.chunks, N = (size_t)p.N;
   fas::PrepassArgs a;
-  a.q = static_cast<const uint16_t*>(q) + H0 * N * D;
-  a.k = static_cast<const uint16_t*>(k) + H0 * N * D;
+  a.q = static_cast<const uint16_t*>(q) + h0 * head_stride();
+  a.k = static_cast<const uint16_t*>(k) + h0 * head_stride();
+  a.row_stride = row_stride();
+  a.head_stride = head_stride();
   a.table = s.table;
   a.partial = s.partial + H0 * Nf * C * D;
   a.mu = s.mu + H0 * D;
@@ -198,14 +212,15 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
 int encode_qkv(const void* q, const void* k, const void* v, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
   const HostPlan& p = g_state.plan;
   const cuuint64_t D = (cuuint64_t)p.d;
+  const cuuint64_t rs = (cuuint64_t)row_stride() * 2, hs = (cuuint64_t)head_stride() * 2;  // bytes
   {
     const cuuint64_t dims[4] = {D, (cuuint64_t)p.T, (cuuint64_t)p.Nf, (cuuint64_t)p.H};
-    const cuuint64_t strides[3] = {D * 2, (cuuint64_t)p.T * D * 2, (cuuint64_t)p.N * D * 2};
+    const cuuint64_t strides[3] = {rs, (cuuint64_t)p.T * rs, hs};
     const cuuint32_t box[4] = {64, (cuuint32_t)fas::kQTile, 1, 1};
     if (encode(tq, q, 4, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
   }
   const cuuint64_t dims[3] = {D, (cuuint64_t)p.N, (cuuint64_t)p.H};
-  const cuuint64_t strides[2] = {D * 2, (cuuint64_t)p.N * D * 2};
+  const cuuint64_t strides[2] = {rs, hs};
   const cuuint32_t box[3] = {64, (cuuint32_t)p.Bk, 1};
   if (encode(tk, k, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
   if (encode(tv, v, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
@@ -223,6 +238,8 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   fp.row_bound = s.row_bound;
   fp.elig = s.elig;
   fp.out = static_cast<uint16_t*>(out);
+  fp.out_row_stride = row_stride();
+  fp.out_head_stride = head_stride();
   fp.lse = lse;
   fp.err = s.err;
   fp.N = p.N;
@@ -232,6 +249,17 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.d));
   fp.limit_ns = fas::kWaitLimitNs;
   return fas::launch_attention(p.d, tq, tk, tv, fp, count, st);
+}
+
+// Copies nh heads of a bf16 q/k/v/out tensor in the current layout; dst and
+// src point at the first head's first element.
+cudaError_t copy_heads(uint16_t* dst, const uint16_t* src, int nh, cudaMemcpyKind kind, cudaStream_t st) {
+  const HostPlan& p = g_state.plan;
+  if (g_state.layout == FAS_LAYOUT_NHD) {
+    const size_t pitch = (size_t)row_stride() * 2, width = (size_t)nh * p.d * 2;
+    return cudaMemcpy2DAsync(dst, pitch, src, pitch, width, (size_t)p.N, kind, st);
+  }
+  return cudaMemcpyAsync(dst, src, (size_t)nh * (size_t)head_stride() * 2, kind, st);
 }
 
 // fas_forward_host resources: device copies of the inputs and outputs, the
@@ -406,7 +434,6 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
   if (rc != FAS_OK) return rc;
   State& s = g_state;
   cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
-  const size_t head_elems = (size_t)p.N * (size_t)p.d;
   const int groups = (p.H + hg - 1) / hg;
   int launches = 0;
   // Start after the caller's earlier work, and after the previous call of
@@ -418,13 +445,14 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
   }
   for (int g = 0; g < groups; ++g) {
     const int h0 = g * hg, nh = (p.H - h0 < hg) ? p.H - h0 : hg;
-    const size_t off = (size_t)h0 * head_elems, n = (size_t)nh * head_elems;
-    // In: q, k, v of the group's heads (contiguous slices of [H, N, d]).
+    // The group's heads: one contiguous slice in [H, N, d]; in [N, H, d] a
+    // slice of every token's row, copied as a 2D block.
+    const size_t off = (size_t)h0 * (size_t)head_stride();
     const void* src[3] = {q, k, v};
     uint16_t* dst[3] = {s.dq, s.dk, s.dv};
     for (int t = 0; t < 3; ++t)
-      if (cudaMemcpyAsync(dst[t] + off, static_cast<const uint16_t*>(src[t]) + off, n * 2, cudaMemcpyHostToDevice,
-                          s.st_h2d) != cudaSuccess)
+      if (copy_heads(dst[t] + off, static_cast<const uint16_t*>(src[t]) + off, nh, cudaMemcpyHostToDevice,
+                     s.st_h2d) != cudaSuccess)
         return FAS_ERR_CUDA;
     if (cudaEventRecord(s.ev_in[g], s.st_h2d) != cudaSuccess) return FAS_ERR_CUDA;
     // Compute: prepass and attention for the group's heads.
@@ -439,7 +467,7 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
     if (cudaEventRecord(s.ev_done[g], s.st_comp) != cudaSuccess) return FAS_ERR_CUDA;
     // Out: the group's rows of out and lse.
     if (cudaStreamWaitEvent(s.st_d2h, s.ev_done[g], 0) != cudaSuccess) return FAS_ERR_CUDA;
-    if (cudaMemcpyAsync(static_cast<uint16_t*>(out) + off, s.dout + off, n * 2, cudaMemcpyDeviceToHost, s.st_d2h) !=
+    if (copy_heads(static_cast<uint16_t*>(out) + off, s.dout + off, nh, cudaMemcpyDeviceToHost, s.st_d2h) !=
             cudaSuccess ||
         cudaMemcpyAsync(lse + (size_t)h0 * p.N, s.dlse + (size_t)h0 * p.N, (size_t)nh * p.N * 4,
                         cudaMemcpyDeviceToHost, s.st_d2h) != cudaSuccess)
@@ -452,6 +480,21 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
   s.pre_q = s.dq;
   s.pre_k = s.dk;
   s.last_launches = launches;
+  return FAS_OK;
+}
+
+int fas_set_layout(int layout) {
+  if (layout != FAS_LAYOUT_HND && layout != FAS_LAYOUT_NHD) return FAS_ERR_ARG;
+  if (!g_state.planned) return FAS_ERR_STATE;
+  if (layout != g_state.layout) {
+    g_state.layout = layout;
+    // The host pipeline's tensor maps and the last prepass belong to the
+    // old layout.
+    if (g_state.io && encode_qkv(g_state.dq, g_state.dk, g_state.dv, &g_state.io_tq, &g_state.io_tk,
+                                 &g_state.io_tv) != FAS_OK)
+      return FAS_ERR_CUDA;
+    g_state.pre_q = g_state.pre_k = nullptr;
+  }
   return FAS_OK;
 }
 

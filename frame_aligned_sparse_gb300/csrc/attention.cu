@@ -473,7 +473,7 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   if (!ok) return;
   ptx::tc_fence_after_sync();
   const float inv = 1.0f / lw;
-  uint16_t* orow = p.out + grow * D;
+  uint16_t* orow = p.out + (int64_t)h * p.out_head_stride + ((int64_t)f * p.T + row) * p.out_row_stride;
   constexpr int kOutChunks = D / 16 / kGroups;
 #pragma unroll 1
   for (int c = g * kOutChunks; c < (g + 1) * kOutChunks; ++c) {

@@ -18,8 +18,10 @@ constexpr unsigned int kErrWaitSelftest = 16u;
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
 
 struct PrepassArgs {
-  const void* q;        // bf16 [H, N, d]
-  const void* k;        // bf16 [H, N, d]
+  const void* q;        // bf16, row (h, j) at q + h * head_stride + j * row_stride
+  const void* k;        // bf16, same layout as q
+  int64_t row_stride;   // elements between consecutive tokens of one head
+  int64_t head_stride;  // elements between heads
   const int4* table;    // [Nf] {start0, len0, start1, len1}
   float* partial;       // [H, Nf, chunks, d]  per-chunk key sums
   float* mu;            // [H, d]              mean key
@@ -51,7 +53,9 @@ struct FwdParams {
   const int4* table;       // [Nf] {start0, len0, start1, len1}
   const float* row_bound;  // [H, N] or null (online mode)
   const uint8_t* elig;     // [H] or null (online mode)
-  uint16_t* out;           // bf16 [H, N, d]
+  uint16_t* out;           // bf16, row (h, j) at out + h * out_head_stride + j * out_row_stride
+  int64_t out_row_stride;  // elements
+  int64_t out_head_stride; // elements
   float* lse;              // [H, N]
   unsigned int* err;       // device error word
   int64_t N;

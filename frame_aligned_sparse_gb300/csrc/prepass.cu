@@ -14,8 +14,11 @@
 // Since the mean of the visible centred logits is at most their maximum,
 // G_i bounds the gap between b_i and the true centred row maximum.
 //
-// All loads are 16-byte vectors, one row shared by d/8 consecutive lanes,
-// consecutive rows over the block: fully coalesced.  Every reduction runs in
+// All loads are 16-byte vectors, one row shared by d/8 consecutive lanes
+// (each row's d values are contiguous), consecutive rows over the block.
+// Rows of one head are row_stride elements apart: d in the head-major
+// [H, N, d] layout (fully contiguous), H*d in the token-major [N, H, d]
+// layout (one 2d-byte segment per row).  Every reduction runs in
 // a fixed order (no floating-point atomics), so results are bit-reproducible.
 
 #include <cuda_runtime.h>
@@ -64,7 +67,8 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
 template <int D>
 __global__ void __launch_bounds__(kPrepassThreads) key_chunk_sums(const uint4* __restrict__ k,
                                                                   float* __restrict__ partial, int64_t N,
-                                                                  int T, int Nf, int chunks) {
+                                                                  int64_t rstride, int64_t hstride, int T,
+                                                                  int Nf, int chunks) {
   constexpr int VPR = D / 8;                   // 16-byte vectors per row
   constexpr int RPI = kPrepassThreads / VPR;   // rows per sweep
   __shared__ float red[RPI][D];
@@ -72,13 +76,13 @@ __global__ void __launch_bounds__(kPrepassThreads) key_chunk_sums(const uint4* _
   const int v = threadIdx.x % VPR, rs = threadIdx.x / VPR;
   const int row0 = c * kPrepassRows;
   const int rows = min(kPrepassRows, T - row0);
-  const uint4* base = k + ((int64_t)h * N + (int64_t)g * T + row0) * VPR + v;
+  const uint4* base = k + (int64_t)h * hstride + ((int64_t)g * T + row0) * rstride + v;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int r = rs;
   for (; r + 3 * RPI < rows; r += 4 * RPI) {
     uint4 x[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = ld_stream(base + (int64_t)(r + u * RPI) * VPR);
+    for (int u = 0; u < 4; ++u) x[u] = ld_stream(base + (int64_t)(r + u * RPI) * rstride);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       float f[8];
@@ -89,7 +93,7 @@ __global__ void __launch_bounds__(kPrepassThreads) key_chunk_sums(const uint4* _
   }
   for (; r < rows; r += RPI) {
     float f[8];
-    unpack8(ld_stream(base + (int64_t)r * VPR), f);
+    unpack8(ld_stream(base + (int64_t)r * rstride), f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] += f[e];
   }
@@ -123,7 +127,8 @@ __global__ void __launch_bounds__(D) key_frame_sums(const float* __restrict__ pa
 template <int D>
 __global__ void __launch_bounds__(kPrepassThreads) key_centred_max(const uint4* __restrict__ k,
                                                                    const float* __restrict__ mu,
-                                                                   float* __restrict__ mpart, int64_t N, int T,
+                                                                   float* __restrict__ mpart, int64_t N,
+                                                                   int64_t rstride, int64_t hstride, int T,
                                                                    int Nf, int chunks) {
   constexpr int VPR = D / 8;
   constexpr int RPI = kPrepassThreads / VPR;
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(kPrepassThreads) key_centred_max(const uint4* 
   float m[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) m[e] = mu[(int64_t)h * D + v * 8 + e];
-  const uint4* base = k + ((int64_t)h * N + (int64_t)g * T + row0) * VPR + v;
+  const uint4* base = k + (int64_t)h * hstride + ((int64_t)g * T + row0) * rstride + v;
   float best = 0.f;
   // Uniform trip count across the block so the lane shuffles stay converged.
   for (int r0 = 0; r0 < rows; r0 += 2 * RPI) {
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(kPrepassThreads) key_centred_max(const uint4* 
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int r = r0 + u * RPI + rs;
-      x[u] = r < rows ? ld_stream(base + (int64_t)r * VPR) : make_uint4(0, 0, 0, 0);
+      x[u] = r < rows ? ld_stream(base + (int64_t)r * rstride) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -244,7 +249,8 @@ __global__ void __launch_bounds__(kPrepassThreads) query_bounds(const uint4* __r
                                                                 const float* __restrict__ mvis,
                                                                 const float* __restrict__ kbarc,
                                                                 float* __restrict__ row_bound,
-                                                                float* __restrict__ gpart, int64_t N, int T,
+                                                                float* __restrict__ gpart, int64_t N,
+                                                                int64_t rstride, int64_t hstride, int T,
                                                                 int Nf, int chunks, float scale) {
   constexpr int VPR = D / 8;
   constexpr int RPI = kPrepassThreads / VPR;
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(kPrepassThreads) query_bounds(const uint4* __r
     kb[e] = kbarc[((int64_t)h * Nf + g) * D + v * 8 + e];
   }
   const float Mv = mvis[(int64_t)h * Nf + g];
-  const uint4* base = q + ((int64_t)h * N + (int64_t)g * T + row0) * VPR + v;
+  const uint4* base = q + (int64_t)h * hstride + ((int64_t)g * T + row0) * rstride + v;
   float* out = row_bound + (int64_t)h * N + (int64_t)g * T + row0;
   float gmax = -INFINITY;
   for (int r0 = 0; r0 < rows; r0 += 2 * RPI) {
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kPrepassThreads) query_bounds(const uint4* __r
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int r = r0 + u * RPI + rs;
-      x[u] = r < rows ? ld_stream(base + (int64_t)r * VPR) : make_uint4(0, 0, 0, 0);
+      x[u] = r < rows ? ld_stream(base + (int64_t)r * rstride) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -315,18 +321,20 @@ int launch_prepass_d(const PrepassArgs& a, cudaStream_t st) {
   const dim3 grid(a.chunks, a.Nf, a.H);
   const uint4* q = static_cast<const uint4*>(a.q);
   const uint4* k = static_cast<const uint4*>(a.k);
+  const int64_t rstride = a.row_stride / 8, hstride = a.head_stride / 8;  // in 16-byte vectors
   int n = 0;
-  key_chunk_sums<D><<<grid, kPrepassThreads, 0, st>>>(k, a.partial, a.N, a.T, a.Nf, a.chunks);
+  key_chunk_sums<D><<<grid, kPrepassThreads, 0, st>>>(k, a.partial, a.N, rstride, hstride, a.T, a.Nf, a.chunks);
   ++n;
   key_frame_sums<D><<<a.H, D, 0, st>>>(a.partial, a.fsum, a.mu, a.N, a.Nf, a.chunks);
   ++n;
-  key_centred_max<D><<<grid, kPrepassThreads, 0, st>>>(k, a.mu, a.mpart, a.N, a.T, a.Nf, a.chunks);
+  key_centred_max<D><<<grid, kPrepassThreads, 0, st>>>(k, a.mu, a.mpart, a.N, rstride, hstride, a.T, a.Nf,
+                                                      a.chunks);
   ++n;
   window_stats<D><<<a.H, D, 0, st>>>(a.mpart, a.fsum, a.mu, a.table, a.frame_max, a.mvis, a.kbarc, a.T, a.Nf,
                                      a.chunks);
   ++n;
-  query_bounds<D><<<grid, kPrepassThreads, 0, st>>>(q, a.mu, a.mvis, a.kbarc, a.row_bound, a.gpart, a.N, a.T,
-                                                    a.Nf, a.chunks, a.scale);
+  query_bounds<D><<<grid, kPrepassThreads, 0, st>>>(q, a.mu, a.mvis, a.kbarc, a.row_bound, a.gpart, a.N, rstride,
+                                                    hstride, a.T, a.Nf, a.chunks, a.scale);
   ++n;
   const int blocks = (a.H + 255) / 256;
   eligibility<<<blocks, 256, 0, st>>>(a.gpart, a.stat, a.elig, a.H, a.Nf * a.chunks);
@@ -340,18 +348,20 @@ int launch_prepass_rule_d(const PrepassArgs& a, int R0, int r, cudaStream_t st) 
   const dim3 grid(a.chunks, a.Nf, a.H);
   const uint4* q = static_cast<const uint4*>(a.q);
   const uint4* k = static_cast<const uint4*>(a.k);
+  const int64_t rstride = a.row_stride / 8, hstride = a.head_stride / 8;  // in 16-byte vectors
   int n = 0;
-  key_chunk_sums<D><<<grid, kPrepassThreads, 0, st>>>(k, a.partial, a.N, a.T, a.Nf, a.chunks);
+  key_chunk_sums<D><<<grid, kPrepassThreads, 0, st>>>(k, a.partial, a.N, rstride, hstride, a.T, a.Nf, a.chunks);
   ++n;
   key_frame_sums<D><<<a.H, D, 0, st>>>(a.partial, a.fsum, a.mu, a.N, a.Nf, a.chunks);
   ++n;
-  key_centred_max<D><<<grid, kPrepassThreads, 0, st>>>(k, a.mu, a.mpart, a.N, a.T, a.Nf, a.chunks);
+  key_centred_max<D><<<grid, kPrepassThreads, 0, st>>>(k, a.mu, a.mpart, a.N, rstride, hstride, a.T, a.Nf,
+                                                      a.chunks);
   ++n;
   window_stats_rule<D><<<a.H, D, 0, st>>>(a.mpart, a.fsum, a.mu, a.frame_max, a.mvis, a.kbarc, a.T, a.Nf, a.chunks,
                                           R0, r);
   ++n;
-  query_bounds<D><<<grid, kPrepassThreads, 0, st>>>(q, a.mu, a.mvis, a.kbarc, a.row_bound, a.gpart, a.N, a.T,
-                                                    a.Nf, a.chunks, a.scale);
+  query_bounds<D><<<grid, kPrepassThreads, 0, st>>>(q, a.mu, a.mvis, a.kbarc, a.row_bound, a.gpart, a.N, rstride,
+                                                    hstride, a.T, a.Nf, a.chunks, a.scale);
   ++n;
   const int blocks = (a.H + 255) / 256;
   eligibility<<<blocks, 256, 0, st>>>(a.gpart, a.stat, a.elig, a.H, a.Nf * a.chunks);

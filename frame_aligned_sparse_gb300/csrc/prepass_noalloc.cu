@@ -80,6 +80,8 @@ extern "C" int fas_prepass_noalloc(const void* q, const void* k, int frame_token
   PrepassArgs a;
   a.q = q;
   a.k = k;
+  a.row_stride = d;                 // head-major [H, N, d]
+  a.head_stride = (int64_t)N * d;
   a.table = nullptr;
   a.partial = part[0];
   a.mu = part[1];

@@ -25,9 +25,12 @@
  *   - frames 0..R0-1 and max(R0, f-r)..min(Nf-1, f+r), if f >= R0.
  *
  * Data layout (all device pointers, owned by the caller):
- *   q, k, v, out : bf16, contiguous [H, N, d], base 16-byte aligned;
- *   lse          : fp32, contiguous [H, N] (natural log of the sum of
- *                  exp(s * q.k) over the visible keys, s = 1/sqrt(d)).
+ *   q, k, v, out : bf16, base 16-byte aligned, contiguous [H, N, d] (the
+ *                  default, FAS_LAYOUT_HND) or, after
+ *                  fas_set_layout(FAS_LAYOUT_NHD), contiguous [N, H, d];
+ *   lse          : fp32, contiguous [H, N] in both layouts (natural log of
+ *                  the sum of exp(s * q.k) over the visible keys,
+ *                  s = 1/sqrt(d)).
  * Batch is folded into H: every head is independent.
  *
  * State.  The library holds one plan at a time (not thread-safe).  fas_plan
@@ -62,6 +65,11 @@ enum {
   FAS_ERR_TIMEOUT = -5,     /* a bounded device-side wait expired */
   FAS_ERR_UNSUPPORTED = -6, /* valid request this build does not support */
   FAS_ERR_SCRATCH = -7      /* problem needs more than fas_prepass_noalloc's fixed scratch */
+};
+
+enum {
+  FAS_LAYOUT_HND = 0, /* q, k, v, out contiguous [H, N, d] (head-major) */
+  FAS_LAYOUT_NHD = 1  /* q, k, v, out contiguous [N, H, d] (token-major) */
 };
 
 enum {
@@ -153,6 +161,19 @@ int fas_forward(const void* q, const void* k, const void* v, void* out, float* l
  * statistics. */
 int fas_forward_host(const void* q, const void* k, const void* v, void* out, float* lse,
                      int mode, int heads_per_group, void* cuda_stream);
+
+/* Memory layout of q, k, v and out for the calls that follow, on the
+ * current plan: FAS_LAYOUT_HND ([H, N, d], the default of every new plan) or
+ * FAS_LAYOUT_NHD ([N, H, d]: the tokens' rows of all heads side by side, as
+ * a fused QKV projection writes them, so no transpose is needed before the
+ * call).  The kernels read and write the strided layout directly (TMA
+ * tensor maps with the layout's strides, strided prepass rows and output
+ * stores); results are bit-identical to the same data in [H, N, d].  lse is
+ * [H, N] in both layouts.  fas_forward_host takes host buffers in the same
+ * layout.  A layout change invalidates the last prepass (AUTO and BOUNDED
+ * need a new fas_prepass).  Needs a plan (FAS_ERR_STATE); an unknown layout
+ * returns FAS_ERR_ARG. */
+int fas_set_layout(int layout);
 
 /* Release every library-owned device buffer and forget the plan. */
 int fas_free(void);

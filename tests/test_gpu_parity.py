@@ -281,3 +281,73 @@ def test_forward_host_argument_errors():
     assert lib.fas_forward_host(None, *p[1:], 0, 0, st) == fas.FAS_ERR_ARG
     with pytest.raises(TypeError):
         fas.fas_forward_host(c.q, c.k, c.v)  # device tensors are refused
+
+
+def to_nhd(bits):
+    """[H, N, d] bf16 bits -> contiguous [N, H, d]."""
+    return np.ascontiguousarray(bits.transpose(1, 0, 2))
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_token_major_layout_matches_head_major(name):
+    """q, k, v, out as [N, H, d] (fas_set_layout nhd): the kernels read and
+    write the strided layout directly, so the results must be bit-identical
+    to the head-major path on the same data, through both the device and
+    the host-buffer entry points."""
+    c = case(name)
+    qn, kn, vn = (to_dev(to_nhd(c.x[t])) for t in "qkv")
+    for mode in ("auto", "online"):
+        elig_h, out_h, lse_h = c.run(mode)
+        out_h, lse_h = out_h.cpu(), lse_h.cpu()
+        fas.fas_set_layout("nhd")
+        elig_n = fas.fas_prepass(qn, kn, want_elig=True)
+        out_n, lse_n = fas.fas_forward(qn, kn, vn, mode=mode)
+        assert fas.fas_status() == fas.FAS_OK
+        assert out_n.shape == (c.w.tokens, c.w.heads, c.w.head_dim)
+        assert np.array_equal(elig_n, elig_h)
+        assert torch.equal(out_n.cpu().transpose(0, 1).contiguous().view(torch.int16), out_h.view(torch.int16))
+        assert torch.equal(lse_n.cpu().view(torch.int32), lse_h.view(torch.int32))
+        hq, hk, hv = (host_bf16(to_nhd(c.x[t])) for t in "qkv")
+        for hg in (0, 1):
+            o2, l2 = fas.fas_forward_host(hq, hk, hv, mode=mode, heads_per_group=hg)
+            torch.cuda.current_stream().synchronize()
+            assert fas.fas_status() == fas.FAS_OK
+            assert torch.equal(o2.transpose(0, 1).contiguous().view(torch.int16), out_h.view(torch.int16)), hg
+            assert torch.equal(l2.view(torch.int32), lse_h.view(torch.int32)), hg
+        fas.fas_set_layout("hnd")
+    c.check(out_n.cpu().transpose(0, 1).contiguous(), lse_n, f"{name}/nhd")
+
+
+def test_token_major_layout_720p_sampled_rows():
+    """The token-major layout on the full 720p SR chunk against the oracle."""
+    c = case("720p")
+    c.plan()
+    fas.fas_set_layout("nhd")
+    try:
+        qn, kn, vn = (to_dev(to_nhd(c.x[t])) for t in "qkv")
+        elig = fas.fas_prepass(qn, kn, want_elig=True)
+        want = np.ones(c.w.heads, dtype=bool)
+        want[c.x["modified_heads"]] = False
+        assert np.array_equal(elig.astype(bool), want)
+        out, lse = fas.fas_forward(qn, kn, vn, mode="auto")
+        assert fas.fas_status() == fas.FAS_OK
+        c.check(out.transpose(0, 1).contiguous(), lse, "720p/nhd")
+    finally:
+        fas.fas_set_layout("hnd")
+
+
+def test_layout_errors():
+    c = case("tiny")
+    c.plan()
+    lib = fas.load()
+    assert lib.fas_set_layout(2) == fas.FAS_ERR_ARG
+    fas.fas_prepass(c.q, c.k)
+    assert lib.fas_set_layout(1) == fas.FAS_OK
+    st = torch.cuda.current_stream().cuda_stream
+    out = torch.empty_like(c.q)
+    lse = torch.empty(c.w.heads, c.w.tokens, device="cuda")
+    # A layout change invalidates the prepass: AUTO needs a new one.
+    assert lib.fas_forward(c.q.data_ptr(), c.k.data_ptr(), c.v.data_ptr(), out.data_ptr(), lse.data_ptr(), 0,
+                           st) == fas.FAS_ERR_STATE
+    assert lib.fas_set_layout(0) == fas.FAS_OK
+    fas.fas_set_layout("hnd")

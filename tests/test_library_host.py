@@ -127,6 +127,8 @@ def test_calls_out_of_order_return_state_error():
     assert lib.fas_prepass(None, None, None, None) == fas.FAS_ERR_STATE
     assert lib.fas_forward(None, None, None, None, None, 0, None) == fas.FAS_ERR_STATE
     assert lib.fas_forward_host(None, None, None, None, None, 0, 0, None) == fas.FAS_ERR_STATE
+    assert lib.fas_set_layout(1) == fas.FAS_ERR_STATE
+    assert lib.fas_set_layout(5) == fas.FAS_ERR_ARG
     assert lib.fas_status(None) == fas.FAS_ERR_STATE
     assert lib.fas_prepass_readback(None, None, None, None, None, None) == fas.FAS_ERR_STATE
     assert lib.fas_selftest_wait_timeout(0, None) == fas.FAS_ERR_ARG
