@@ -87,6 +87,9 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("stress", 24, 128, 1, 21, 3600, 2, 3.0, 4, "heavy", 12),
         # Same tensors as "stress" (same seed and modifier); every frame visible.
         Workload("dense", 24, 128, 1, 21, 3600, 21, 3.0, 4, "heavy", 12),
+        # The 720p geometry with 4 heads (0.24 GB of Q/K/V, still larger than
+        # L2): small enough for multi-pass profiler captures.
+        Workload("720p_h4", 4, 128, 1, 21, 3600, 2, 3.0, 5),
     ]
 }
 
