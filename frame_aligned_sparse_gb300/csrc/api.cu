@@ -49,7 +49,8 @@ struct State {
   float* dlse = nullptr;
   CUtensorMap io_tq{}, io_tk{}, io_tv{};
   int4* gwork = nullptr;
-  int gwork_hg = 0;                  // heads per group the regrouped list was built for
+  int gwork_hg = -1;                 // heads_per_group argument the regrouped list was built for
+  std::vector<int> grp_h0;           // first head of each group (plus H)
   std::vector<int> gwork_off;        // first item of each group (plus the end)
   cudaStream_t st_h2d = nullptr, st_comp = nullptr, st_d2h = nullptr;
   std::vector<cudaEvent_t> ev_in, ev_done;
@@ -59,10 +60,32 @@ struct State {
 
 State g_state;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-// Default heads per group of fas_forward_host: small enough that the first
-// group's copy-in and the last group's copy-out are short, large enough
-// that each group's attention launch fills the GPU many times over.
+// Heads per group of fas_forward_host's default schedule in steady state:
+// large enough that each group's attention launch fills the GPU many times
+// over.  The schedule ramps up to it (1, 2, 4, ... heads) so that the first
+// copy-in, which nothing hides, is one head, and each group's copy-in takes
+// about as long as the previous group's compute; it ends with a one-head
+// group so that the last copy-out is short too.
 constexpr int kHostGroupHeads = 4;
+
+// Group boundaries (first head of each group, then H) for heads_per_group
+// hg > 0 (uniform groups) or 0 (the ramped default schedule).
+std::vector<int> head_groups(int H, int hg) {
+  std::vector<int> b(1, 0);
+  if (hg > 0) {
+    for (int h = hg; h < H; h += hg) b.push_back(h);
+  } else if (H > 2) {
+    // 1, 2, 4, 4, ... heads over the first H - 1 heads, then one head.
+    int h = 0, size = 1;
+    while (h < H - 1) {
+      h += (H - 1 - h < size) ? H - 1 - h : size;
+      b.push_back(h);
+      if (size < kHostGroupHeads) size *= 2;
+    }
+  }
+  b.push_back(H);
+  return b;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -289,13 +312,14 @@ int ensure_host_pipeline(int hg) {
     for (cudaEvent_t* e : {&s.ev_entry, &s.ev_exit})
       if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
   }
-  const int groups = (p.H + hg - 1) / hg;
+  if (s.gwork_hg != hg) s.grp_h0 = head_groups(p.H, hg);
+  const int groups = (int)s.grp_h0.size() - 1;
   while ((int)s.ev_in.size() < groups) {
-    cudaEvent_t a = nullptr, b = nullptr;
-    if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
-    s.ev_in.push_back(a);
-    if (cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
-    s.ev_done.push_back(b);
+    for (auto* evs : {&s.ev_in, &s.ev_done}) {
+      cudaEvent_t e = nullptr;
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
+      evs->push_back(e);
+    }
   }
   if (s.gwork_hg != hg) {
     // The plan's list is heaviest first over all heads; keeping that order
@@ -305,7 +329,8 @@ int ensure_host_pipeline(int hg) {
     s.gwork_off.assign(1, 0);
     for (int g = 0; g < groups; ++g) {
       for (size_t i = 0; i < p.work.size(); i += 4)
-        if (p.work[i] / hg == g) grouped.insert(grouped.end(), p.work.begin() + i, p.work.begin() + i + 4);
+        if (p.work[i] >= s.grp_h0[g] && p.work[i] < s.grp_h0[g + 1])
+          grouped.insert(grouped.end(), p.work.begin() + i, p.work.begin() + i + 4);
       s.gwork_off.push_back((int)(grouped.size() / 4));
     }
     if (!s.gwork && cudaMalloc(&s.gwork, p.work.size() * 4) != cudaSuccess) {
@@ -425,7 +450,7 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
   if (mode != FAS_MODE_AUTO && mode != FAS_MODE_ONLINE && mode != FAS_MODE_BOUNDED) return FAS_ERR_ARG;
   const HostPlan& p = g_state.plan;
   if (heads_per_group < 0 || heads_per_group > p.H) return FAS_ERR_ARG;
-  const int hg = heads_per_group > 0 ? heads_per_group : (p.H < kHostGroupHeads ? p.H : kHostGroupHeads);
+  const int hg = heads_per_group;
   int rc = check_device();
   if (rc != FAS_OK) return rc;
   rc = ensure_encoder();
@@ -434,7 +459,7 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
   if (rc != FAS_OK) return rc;
   State& s = g_state;
   cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
-  const int groups = (p.H + hg - 1) / hg;
+  const int groups = (int)s.grp_h0.size() - 1;
   int launches = 0;
   // Start after the caller's earlier work, and after the previous call of
   // this function has finished with the library's device copies.
@@ -443,10 +468,14 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
     if (cudaStreamWaitEvent(st, s.ev_entry, 0) != cudaSuccess) return FAS_ERR_CUDA;
     if (s.exit_recorded && cudaStreamWaitEvent(st, s.ev_exit, 0) != cudaSuccess) return FAS_ERR_CUDA;
   }
+  // Work is submitted stream by stream (all copies in, then all compute,
+  // then all copies out): a copy-out that waits for its group's compute
+  // must never sit ahead of a later group's copy-in in a hardware queue the
+  // two directions might share.
   for (int g = 0; g < groups; ++g) {
-    const int h0 = g * hg, nh = (p.H - h0 < hg) ? p.H - h0 : hg;
-    // The group's heads: one contiguous slice in [H, N, d]; in [N, H, d] a
-    // slice of every token's row, copied as a 2D block.
+    // In: the group's heads, one contiguous slice in [H, N, d]; in [N, H, d]
+    // a slice of every token's row, copied as a 2D block.
+    const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
     const size_t off = (size_t)h0 * (size_t)head_stride();
     const void* src[3] = {q, k, v};
     uint16_t* dst[3] = {s.dq, s.dk, s.dv};
@@ -455,7 +484,10 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
                      s.st_h2d) != cudaSuccess)
         return FAS_ERR_CUDA;
     if (cudaEventRecord(s.ev_in[g], s.st_h2d) != cudaSuccess) return FAS_ERR_CUDA;
+  }
+  for (int g = 0; g < groups; ++g) {
     // Compute: prepass and attention for the group's heads.
+    const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
     if (cudaStreamWaitEvent(s.st_comp, s.ev_in[g], 0) != cudaSuccess) return FAS_ERR_CUDA;
     const int np = fas::launch_prepass(prepass_args(s.dq, s.dk, h0, nh), s.st_comp);
     if (np < 0) return FAS_ERR_CUDA;
@@ -465,7 +497,11 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
       return FAS_ERR_CUDA;
     ++launches;
     if (cudaEventRecord(s.ev_done[g], s.st_comp) != cudaSuccess) return FAS_ERR_CUDA;
+  }
+  for (int g = 0; g < groups; ++g) {
     // Out: the group's rows of out and lse.
+    const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
+    const size_t off = (size_t)h0 * (size_t)head_stride();
     if (cudaStreamWaitEvent(s.st_d2h, s.ev_done[g], 0) != cudaSuccess) return FAS_ERR_CUDA;
     if (copy_heads(static_cast<uint16_t*>(out) + off, s.dout + off, nh, cudaMemcpyDeviceToHost, s.st_d2h) !=
             cudaSuccess ||

@@ -144,10 +144,13 @@ int fas_forward(const void* q, const void* k, const void* v, void* out, float* l
  * when its activations live on the host.  q, k, v, out: host bf16 [H, N, d];
  * lse: host fp32 [H, N]; layouts and results as for fas_prepass followed by
  * fas_forward (bit-identical outputs).  The heads are independent, so the
- * call splits them into groups of heads_per_group (0 = library default, 4)
- * and pipelines the groups on three library-owned streams: while group g
- * is computed (prepass and attention), group g+1 is copied in and group g-1
- * copied out.  The host buffers should be page-locked (cudaHostAlloc or
+ * call splits them into groups and pipelines the groups on three
+ * library-owned streams: while group g is computed (prepass and attention),
+ * group g+1 is copied in and group g-1 copied out.  heads_per_group > 0
+ * gives groups of that many heads; 0 gives the default schedule, which
+ * ramps up (1, 2, then 4 heads per group) so that the first copy-in, which
+ * nothing hides, is short, and ends with a one-head group so that the last
+ * copy-out is short too.  The host buffers should be page-locked (cudaHostAlloc or
  * cudaHostRegister); pageable buffers give correct results without the
  * overlap.  On first use per plan the library allocates device copies of
  * q, k, v, out and lse (4*H*N*d*2 + 4*H*N bytes, released by fas_free or

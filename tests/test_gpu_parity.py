@@ -351,3 +351,29 @@ def test_layout_errors():
                            st) == fas.FAS_ERR_STATE
     assert lib.fas_set_layout(0) == fas.FAS_OK
     fas.fas_set_layout("hnd")
+
+
+def test_forward_host_back_to_back_calls():
+    """Consecutive fas_forward_host calls overlap on the library's streams
+    (one call's copy-in under the previous call's last head groups), with
+    per-group ordering on the shared device copies.  Three calls on two
+    different inputs, with no synchronisation in between, must each give
+    the device path's result for their own inputs."""
+    c = case("mid")
+    c.plan()
+    xa = c.x
+    xb = {t: xa[t][::-1].copy() for t in "qkv"}  # heads in reverse order: other data per head
+    ha = [host_bf16(xa[t]) for t in "qkv"]
+    hb = [host_bf16(xb[t]) for t in "qkv"]
+    outs = []
+    for h in (ha, hb, ha):
+        outs.append(fas.fas_forward_host(*h, mode="auto"))
+    torch.cuda.current_stream().synchronize()
+    assert fas.fas_status() == fas.FAS_OK
+    for x, (o, l) in zip((xa, xb, xa), outs):
+        q, k, v = (to_dev(x[t]) for t in "qkv")
+        fas.fas_prepass(q, k)
+        od, ld = fas.fas_forward(q, k, v, mode="auto")
+        assert fas.fas_status() == fas.FAS_OK
+        assert torch.equal(o.view(torch.int16), od.cpu().view(torch.int16))
+        assert torch.equal(l.view(torch.int32), ld.cpu().view(torch.int32))
