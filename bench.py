@@ -329,7 +329,8 @@ def run_fas(args, w):
         plan()
         fas.fas_forward_host(pin["q"], pin["k"], pin["v"], out_h, lse_h, mode=args.mode, stream=stream)
 
-    e2e_step()
+    for _ in range(3):  # first use builds the host pipeline and touches the pinned buffers
+        e2e_step()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
