@@ -71,7 +71,7 @@ constexpr float kRescaleThreshold = 8.0f;
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t q_tmem;  // Q copied into TMEM (used when Q lives in TMEM)
+  uint64_t q_tmem;  // Q copied into TMEM, the Q slot free (used when Q lives in TMEM)
   uint64_t k_full[kMaxStages];
   uint64_t k_empty[kMaxStages];
   uint64_t v_full[kMaxStages];
@@ -182,8 +182,18 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
   const uint64_t kdesc_qslot = ptx::smem_desc_sw128(q_s, 16, 1024);
   const uint64_t qdesc = ptx::smem_desc_sw128(q_s, 16, 1024);
   const uint64_t vdesc0 = ptx::smem_desc_sw128(v_s0, kHalfBytes, 1024);
-  bool ok = ptx::mbar_wait<true>(ptx::smem_addr(kQTmem ? &bars.q_tmem : &bars.q_full), 0, abort_flag, p.err,
-                                 kErrWaitMma, p.limit_ns);
+  bool ok = ptx::mbar_wait<false>(ptx::smem_addr(&bars.q_full), 0, abort_flag, p.err, kErrWaitMma, p.limit_ns);
+  if (ok && kQTmem) {
+    // Q into TMEM: one 128-lane x 256-bit copy per 16-column K slice of the
+    // 128B-swizzled tile, which lands in the A-operand layout of
+    // tcgen05.mma (column c holds elements 2c, 2c+1 of the lane's row).  The
+    // pipe runs the copies before the S MMAs issued after them; the commit
+    // frees the Q slot for the K ring once the copies are done.
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      ptx::tmem_cp_128x256b(tmem + kColQ + kk * 8, qdesc + (((kk >> 2) * (kQTile * 128) + (kk & 3) * 32) >> 4));
+    ptx::mma_commit(ptx::smem_addr(&bars.q_tmem));
+  }
   // Ring positions (stage, phase parity) advanced incrementally.
   int ks = 0, kph = 0, vs = 0, vph = 0;
   // S(j) = Q . K(j)^T : M=128, N=Bk, K=d in d/16 MMAs.
@@ -254,29 +264,6 @@ __device__ __forceinline__ void mma_issuer(Barriers& bars, uint32_t tmem, uint32
   // Every MMA issued above completes before TMEM is released.
   ptx::mma_commit(ptx::smem_addr(&bars.drain));
   drain_wait(ptx::smem_addr(&bars.drain), 0, p.err, p.limit_ns);
-}
-
-// Copies this thread's Q row from the 128B-swizzled shared-memory tile into
-// TMEM as bf16 pairs (column c holds elements 2c, 2c+1), the A-operand layout
-// of tcgen05.mma.  In each 1 KB swizzle atom the 16-byte chunk index of row
-// t is XORed with t mod 8.
-template <int D>
-__device__ __forceinline__ void stage_q_row(uint32_t q_s, uint32_t taddr, int trow) {
-#pragma unroll
-  for (int half = 0; half < D / 64; ++half) {
-    const uint32_t row_addr = q_s + half * (kQTile * 128) + trow * 128;
-    uint32_t w[2][16];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 x = ptx::ld_shared_v4(row_addr + ((uint32_t)(c ^ (trow & 7)) << 4));
-      w[c / 4][(c % 4) * 4 + 0] = x.x;
-      w[c / 4][(c % 4) * 4 + 1] = x.y;
-      w[c / 4][(c % 4) * 4 + 2] = x.z;
-      w[c / 4][(c % 4) * 4 + 3] = x.w;
-    }
-    ptx::tmem_st16(taddr + half * 32, w[0]);
-    ptx::tmem_st16(taddr + half * 32 + 16, w[1]);
-  }
 }
 
 // Of the 8 element pairs of a 16-column chunk, this many take 2^x on the FMA
@@ -381,18 +368,6 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   float l0 = 0.f, l1 = 0.f, w0 = 0.f, w1 = 0.f;
   bool ok = true;
 
-  if (kQTmem && g == 0) {
-    const bool got = ptx::mbar_wait(ptx::smem_addr(&bars.q_full), 0, abort_flag, p.err, kErrWaitSoftmax, p.limit_ns);
-    ok = __all_sync(0xffffffffu, got);
-    if (ok) {
-      stage_q_row<D>(q_s, tmem + lane_base + kColQ, trow);
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before_sync();
-      ptx::fence_proxy_async_smem();  // the Q slot is next written by TMA
-      ptx::mbar_arrive(ptx::smem_addr(&bars.q_tmem));
-    }
-  }
-
   const int j0 = bounded ? g : 0;
   const int jstep = bounded ? kGroups : 1;
   const bool active = bounded || g == 0;
@@ -475,17 +450,20 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
   const float inv = 1.0f / lw;
   uint16_t* orow = p.out + (int64_t)h * p.out_head_stride + ((int64_t)f * p.T + row) * p.out_row_stride;
   constexpr int kOutChunks = D / 16 / kGroups;
-#pragma unroll 1
-  for (int c = g * kOutChunks; c < (g + 1) * kOutChunks; ++c) {
-    uint32_t o[16];
-    ptx::tmem_ld16(tmem + lane_base + kColO + c * 16, o);
-    ptx::tmem_ld_wait(o);
+  // All of the group's O columns are loaded before one wait.
+  uint32_t o[kOutChunks][16];
+#pragma unroll
+  for (int u = 0; u < kOutChunks; ++u) ptx::tmem_ld16(tmem + lane_base + kColO + (g * kOutChunks + u) * 16, o[u]);
+#pragma unroll
+  for (int u = 0; u < kOutChunks; ++u) ptx::tmem_ld_wait(o[u]);
+#pragma unroll
+  for (int u = 0; u < kOutChunks; ++u) {
     uint32_t pk[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      pk[e] = ptx::pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+      pk[e] = ptx::pack_bf16x2(__uint_as_float(o[u][2 * e]) * inv, __uint_as_float(o[u][2 * e + 1]) * inv);
     if (valid) {
-      uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+      uint4* dst = reinterpret_cast<uint4*>(orow + (g * kOutChunks + u) * 16);
       dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
@@ -515,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_addr(&bars.q_full), 1);
-    ptx::mbar_init(ptx::smem_addr(&bars.q_tmem), 32 * 4);  // warpgroup 0
+    ptx::mbar_init(ptx::smem_addr(&bars.q_tmem), 1);  // tcgen05.commit after the Q copy
     for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(ptx::smem_addr(&bars.k_full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&bars.k_empty[s]), 1);

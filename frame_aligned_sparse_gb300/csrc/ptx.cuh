@@ -230,6 +230,15 @@ __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
       : "memory");
 }
 
+// Copy a 128-row x 256-bit slice of a shared-memory matrix (described like
+// an MMA operand) into TMEM lanes 0..127, 8 columns from taddr on.  For a
+// K-major bf16 tile this is the A-operand layout of tcgen05.mma (column c
+// holds elements 2c, 2c+1 of the lane's row).  Runs on the tensor pipe in
+// issue order with this thread's MMAs.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 // Arrive on the mbarrier once every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
