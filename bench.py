@@ -52,6 +52,26 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The job's time is its slowest rank's: MAX all-reduce of one timing
+    (a no-op in a single process).  device: where the reduction tensor lives
+    (the rank's GPU under NCCL, the CPU under gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs its own chunk (replicas, weak
+    scaling), so the job does world * steps chunks in the slowest rank's
+    time."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def visible_flops(w) -> float:
     """4*d per visible pair, from the frame rule (reference global both ways,
     window clipped to the video frames)."""
@@ -307,12 +327,9 @@ def run_fas(args, w):
     timed_launches = launches[0]
     ms_total = t_start.elapsed_time(t_end)
     fwd_ms = [a.elapsed_time(b) for a, b in fwd_events]
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
-    value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+    value = job_tflops(world, flops, args.steps, ms_total)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
     prepass_ms = ms_step - fwd_avg
 
@@ -341,10 +358,7 @@ def run_fas(args, w):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     h2d = sum(pin[t].numel() * 2 for t in "qkv")
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
@@ -379,7 +393,7 @@ def run_fas(args, w):
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                      "traffic": recorded_traffic()},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(world, flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": timed_launches,
         "clocks": clocks,
