@@ -141,18 +141,19 @@ int fas_forward(const void* q, const void* k, const void* v, void* out, float* l
                 int mode, void* cuda_stream);
 
 /* Attention with inputs and outputs in HOST memory: the call a process makes
- * when its activations live on the host.  q, k, v, out: host bf16 [H, N, d];
- * lse: host fp32 [H, N]; layouts and results as for fas_prepass followed by
- * fas_forward (bit-identical outputs).  The heads are independent, so the
+ * when its activations live on the host.  q, k, v, out: host bf16 in the
+ * current layout ([H, N, d], or [N, H, d] after fas_set_layout); lse: host
+ * fp32 [H, N]; results as for fas_prepass followed by fas_forward
+ * (bit-identical outputs).  The heads are independent, so the
  * call splits them into groups and pipelines the groups on three
  * library-owned streams: while group g is computed (prepass and attention),
  * group g+1 is copied in and group g-1 copied out.  heads_per_group > 0
  * gives groups of that many heads; 0 gives the default schedule, which
  * ramps up (1, 2, then 4 heads per group) so that the first copy-in, which
  * nothing hides, is short, and ends with a one-head group so that the last
- * copy-out is short too.  The host buffers should be page-locked (cudaHostAlloc or
- * cudaHostRegister); pageable buffers give correct results without the
- * overlap.  On first use per plan the library allocates device copies of
+ * copy-out is short too.  The host buffers should be page-locked
+ * (cudaHostAlloc or cudaHostRegister); pageable buffers give correct
+ * results without the overlap.  On first use per plan the library allocates device copies of
  * q, k, v, out and lse (4*H*N*d*2 + 4*H*N bytes, released by fas_free or
  * the next fas_plan), creates its streams and events, and regroups the work
  * list.  The work starts after everything already enqueued on cuda_stream
