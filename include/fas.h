@@ -122,8 +122,9 @@ int fas_plan_describe(int frame_tokens, int n_frames, int ref_frames, int window
                       int32_t* table, int32_t* work);
 
 /* Prepass ("Unchaining the Softmax": precomputed norms, mean-centred keys).
- * Reads q and k (device, bf16 [H, N, d]) and computes per head the mean key
- * mu_h, per key frame the largest centred key norm, and per row
+ * Reads q and k (device, bf16, in the current layout: [H, N, d] by
+ * default) and computes per head the mean key mu_h, per key frame the
+ * largest centred key norm, and per row
  *   m_i = s q_i.mu_h + s |q_i| max_{visible frames g} max_{j in g} |k_j - mu_h|
  * (an upper bound on the row's largest scaled logit), plus the eligibility
  * statistic stat_h = max_i (b_i - s q_i.kbar_c(i)) where b_i is the centred
@@ -133,10 +134,11 @@ int fas_plan_describe(int frame_tokens, int n_frames, int ref_frames, int window
  * stream, copies the bits and reports device timeouts. */
 int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_host);
 
-/* Attention.  q, k, v: device bf16 [H, N, d]; out: device bf16 [H, N, d];
- * lse: device fp32 [H, N].  Modes AUTO and BOUNDED need a prior fas_prepass
- * on the same q and k (else FAS_ERR_STATE); ONLINE does not.  Every output
- * row is written exactly once; out rows are rounded to bf16 (nearest even). */
+/* Attention.  q, k, v, out: device bf16 in the current layout ([H, N, d],
+ * or [N, H, d] after fas_set_layout); lse: device fp32 [H, N].  Modes AUTO
+ * and BOUNDED need a prior fas_prepass on the same q and k (else
+ * FAS_ERR_STATE); ONLINE does not.  Every output row is written exactly
+ * once; out rows are rounded to bf16 (nearest even). */
 int fas_forward(const void* q, const void* k, const void* v, void* out, float* lse,
                 int mode, void* cuda_stream);
 
@@ -209,7 +211,8 @@ int fas_selftest_wait_timeout(int limit_us, void* cuda_stream);
  * plan and allocates nothing: its scratch is a fixed array of
  * FAS_NOALLOC_SCRATCH_BYTES in device memory that the library image holds on
  * every GPU that loads it, until the process exits.
- *   q, k       : device bf16 [H, N, d] (as for fas_prepass), 16-byte aligned;
+ *   q, k       : device bf16 [H, N, d] (head-major, whatever the current
+ *                layout of the plan calls), 16-byte aligned;
  *   row_bound  : device fp32 [H, N], receives m_i (as fas_prepass_readback);
  *   stat       : device fp32 [H], receives stat_h;
  *   elig       : device uint8 [H], receives the eligibility bits.
