@@ -70,3 +70,16 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
     monkeypatch.setattr(workloads, "generate", lambda *a, **k: called.append(1))
     assert bench.run_reference(None, workloads.get("720p")) == 0
     assert not called
+
+
+def test_bench_flop_count_matches_oracle_definition():
+    """The benchmark's TFLOP/s divides by visible FLOPs (4*d per visible
+    (query, key) pair); its count must equal the oracle's, from the mask
+    definition, on every workload."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    from oracle import reference as ref
+    for w in workloads.WORKLOADS.values():
+        want = ref.visible_flops(w.heads, w.head_dim, w.frame_tokens, w.n_frames, w.ref_frames, w.window_radius)
+        assert bench.visible_flops(w) == want, w.name
