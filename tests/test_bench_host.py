@@ -1,4 +1,5 @@
-"""The benchmark's multi-rank logic on CPU, with two gloo ranks.
+"""The benchmark's host-side logic on CPU: its multi-rank timing, with two
+gloo ranks, and its FLOP count.
 
 On one GB300 per box the benchmark runs N replicas (one full SR chunk per
 rank, no collective on the data path); what crosses ranks is the timing:
