@@ -41,4 +41,6 @@ from .reference import (  # noqa: F401
     bound_statistics,
     visible_pairs,
     visible_flops,
+    frame_spans,
+    frame_of,
 )

@@ -4,6 +4,10 @@ Notation (all integers are token or frame indices):
 
 * ``T`` tokens per frame; frames ``0 .. R0-1`` are reference frames, frames
   ``R0 .. Nf-1`` are video frames; token ``j`` lies in frame ``j // T``.
+  Wherever a function takes ``frame_tokens`` it also accepts a sequence of
+  per-frame token counts ``T_0 .. T_{Nf-1}`` (frames of different spans,
+  still contiguous and in the same order); token ``j`` then lies in the
+  frame ``g`` with ``T_0 + .. + T_{g-1} <= j < T_0 + .. + T_g``.
 * ``r`` window radius; ``s = 1 / sqrt(d)``.
 
 Readings where the pages are silent (each listed in the design notes):
@@ -49,6 +53,23 @@ def _as_f64(x: np.ndarray) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
+def frame_spans(frame_tokens, n_tokens: int) -> np.ndarray:
+    """Per-frame token counts: ``frame_tokens`` itself when it is a
+    sequence, else ``n_tokens // frame_tokens`` copies of it."""
+    if np.ndim(frame_tokens) == 0:
+        return np.full(n_tokens // int(frame_tokens), int(frame_tokens), dtype=np.int64)
+    spans = np.asarray(frame_tokens, dtype=np.int64)
+    assert spans.sum() == n_tokens, "frame spans must add up to the sequence length"
+    return spans
+
+
+def frame_of(tokens, frame_tokens, n_tokens: int) -> np.ndarray:
+    """Frame index of each token."""
+    spans = frame_spans(frame_tokens, n_tokens)
+    starts = np.cumsum(spans) - spans
+    return np.searchsorted(starts, np.asarray(tokens, dtype=np.int64), side="right") - 1
+
+
 # ---------------------------------------------------------------------------
 # The mask ("Deleting the Mask": window of nearby frames plus one global
 # reference frame; live regions snap to frame boundaries).
@@ -78,22 +99,26 @@ def token_mask(rows: np.ndarray, n_tokens: int, frame_tokens: int,
     ``vis(i, j) = fr(j) < R0  or  fr(i) < R0  or  |fr(i) - fr(j)| <= r``
     (the last clause only between video frames).
     """
-    fi = (np.asarray(rows, dtype=np.int64) // frame_tokens)[:, None]
-    fj = (np.arange(n_tokens, dtype=np.int64) // frame_tokens)[None, :]
+    fi = frame_of(rows, frame_tokens, n_tokens)[:, None]
+    fj = frame_of(np.arange(n_tokens), frame_tokens, n_tokens)[None, :]
     ref_key = fj < ref_frames
     ref_row = fi < ref_frames
     window = (fi >= ref_frames) & (fj >= ref_frames) & (np.abs(fi - fj) <= radius)
     return ref_key | ref_row | window
 
 
-def visible_pairs(frame_tokens: int, n_frames: int, ref_frames: int, radius: int) -> int:
+def visible_pairs(frame_tokens, n_frames: int, ref_frames: int, radius: int) -> int:
     """Number of visible (query, key) pairs for one head (valid rows only)."""
     nf = ref_frames + n_frames
-    frames = sum(len(visible_frames(f, nf, ref_frames, radius)) for f in range(nf))
-    return frames * frame_tokens * frame_tokens
+    if np.ndim(frame_tokens) == 0:
+        frames = sum(len(visible_frames(f, nf, ref_frames, radius)) for f in range(nf))
+        return frames * frame_tokens * frame_tokens
+    spans = [int(t) for t in frame_tokens]
+    assert len(spans) == nf
+    return sum(spans[f] * sum(spans[g] for g in visible_frames(f, nf, ref_frames, radius)) for f in range(nf))
 
 
-def visible_flops(heads: int, head_dim: int, frame_tokens: int, n_frames: int,
+def visible_flops(heads: int, head_dim: int, frame_tokens, n_frames: int,
                   ref_frames: int, radius: int) -> float:
     """4*d FLOPs per visible pair (2*d for q.k, 2*d for p*v)."""
     return 4.0 * head_dim * heads * visible_pairs(frame_tokens, n_frames, ref_frames, radius)
@@ -103,7 +128,7 @@ def visible_flops(heads: int, head_dim: int, frame_tokens: int, n_frames: int,
 # Dense masked attention, the definition the single-pass kernel reaches.
 # ---------------------------------------------------------------------------
 
-def masked_attention(q, k, v, frame_tokens: int, ref_frames: int, radius: int,
+def masked_attention(q, k, v, frame_tokens, ref_frames: int, radius: int,
                      rows: Optional[np.ndarray] = None,
                      heads: Optional[Sequence[int]] = None,
                      slab: int = 256) -> Dict[str, np.ndarray]:
@@ -143,7 +168,7 @@ def masked_attention(q, k, v, frame_tokens: int, ref_frames: int, radius: int,
 # Cauchy-Schwarz bound and per-head eligibility ("Unchaining the Softmax").
 # ---------------------------------------------------------------------------
 
-def bound_statistics(q, k, frame_tokens: int, ref_frames: int, radius: int,
+def bound_statistics(q, k, frame_tokens, ref_frames: int, radius: int,
                      heads: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
     """Bound quantities in fp64 for every row of the selected heads.
 
@@ -165,8 +190,9 @@ def bound_statistics(q, k, frame_tokens: int, ref_frames: int, radius: int,
     ``stat[h] = max_i G_i`` and ``elig[h] = stat[h] <= 32``.
     """
     H, N, d = q.shape
-    T = frame_tokens
-    nf = N // T
+    spans = frame_spans(frame_tokens, N)
+    nf = len(spans)
+    bounds = np.concatenate([[0], np.cumsum(spans)])
     hs = list(range(H)) if heads is None else list(heads)
     s = 1.0 / math.sqrt(d)
     vis = frame_visibility(nf, ref_frames, radius)
@@ -177,11 +203,11 @@ def bound_statistics(q, k, frame_tokens: int, ref_frames: int, radius: int,
         mu = kh.mean(axis=0)
         kc = kh - mu[None, :]
         norms = np.sqrt((kc * kc).sum(axis=1))
-        M = norms.reshape(nf, T).max(axis=1)
-        fsum = kh.reshape(nf, T, d).sum(axis=1)
+        M = np.array([norms[bounds[g]:bounds[g + 1]].max() for g in range(nf)])
+        fsum = np.stack([kh[bounds[g]:bounds[g + 1]].sum(axis=0) for g in range(nf)])
         Mvis = np.array([M[vis[f]].max() for f in range(nf)])
-        kbar_c = np.stack([fsum[vis[f]].sum(axis=0) / (vis[f].sum() * T) - mu for f in range(nf)])
-        fr = np.arange(N) // T
+        kbar_c = np.stack([fsum[vis[f]].sum(axis=0) / spans[vis[f]].sum() - mu for f in range(nf)])
+        fr = frame_of(np.arange(N), spans, N)
         qn = np.sqrt((qh * qh).sum(axis=1))
         c = s * (qh @ mu)
         b = s * qn * Mvis[fr]

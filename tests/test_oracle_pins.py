@@ -331,12 +331,157 @@ def check_bound_on_inputs(o):
 
 
 # ---------------------------------------------------------------------------
+# Frames of different spans (a ragged block table): the same rule over
+# frames, with token j in the frame whose token range holds it.
+# ---------------------------------------------------------------------------
+
+def brute_frame(j, spans):
+    """Frame of token j, by walking the frames' token ranges."""
+    start = 0
+    for g, t in enumerate(spans):
+        if start <= j < start + t:
+            return g
+        start += t
+    raise IndexError(j)
+
+
+RAGGED = [
+    dict(H=2, d=4, R0=1, spans=[3, 2, 5, 1, 4, 2], r=1, seed=41),
+    dict(H=1, d=8, R0=2, spans=[2, 4, 1, 3, 3, 2], r=0, seed=42),
+    dict(H=1, d=4, R0=0, spans=[4, 1, 2, 6, 3], r=2, seed=43),
+    dict(H=1, d=4, R0=1, spans=[5, 2, 3, 1], r=9, seed=44),
+]
+
+
+def ragged_inputs(c, key_shift=3.0):
+    rng = np.random.default_rng(c["seed"])
+    N = sum(c["spans"])
+    q = rng.standard_normal((c["H"], N, c["d"]))
+    k = rng.standard_normal((c["H"], N, c["d"])) + key_shift * rng.standard_normal((c["H"], 1, c["d"]))
+    v = rng.standard_normal((c["H"], N, c["d"]))
+    return q, k, v
+
+
+def brute_attention_ragged(q, k, v, spans, R0, r):
+    N, d = len(q), len(q[0])
+    s = 1.0 / math.sqrt(d)
+    outs, lses = [], []
+    for i in range(N):
+        logits = [(j, s * sum(q[i][c] * k[j][c] for c in range(d))) for j in range(N)
+                  if brute_sees(brute_frame(i, spans), brute_frame(j, spans), R0, r)]
+        zmax = max(z for _, z in logits)
+        tot = sum(math.exp(z - zmax) for _, z in logits)
+        out = [sum(math.exp(z - zmax) / tot * v[j][c] for j, z in logits) for c in range(d)]
+        outs.append(out)
+        lses.append(zmax + math.log(tot))
+    return np.array(outs), np.array(lses)
+
+
+def check_ragged_token_mask(o):
+    for c in RAGGED:
+        spans, N = c["spans"], sum(c["spans"])
+        F = len(spans) - c["R0"]
+        got = o.token_mask(np.arange(N), N, spans, c["R0"], c["r"])
+        for i in range(N):
+            for j in range(N):
+                want = brute_sees(brute_frame(i, spans), brute_frame(j, spans), c["R0"], c["r"])
+                assert got[i, j] == want, (c, i, j)
+        assert got.sum() == o.visible_pairs(spans, F, c["R0"], c["r"])
+
+
+def check_ragged_attention_brute(o):
+    for c in RAGGED:
+        q, k, v = ragged_inputs(c)
+        res = o.masked_attention(q, k, v, c["spans"], c["R0"], c["r"])
+        for h in range(c["H"]):
+            out, lse = brute_attention_ragged(q[h].tolist(), k[h].tolist(), v[h].tolist(), c["spans"], c["R0"],
+                                              c["r"])
+            np.testing.assert_allclose(res["out"][h], out, rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(res["lse"][h], lse, rtol=1e-12, atol=1e-12)
+
+
+def check_ragged_bound_stats_brute(o):
+    for c in RAGGED:
+        q, k, _ = ragged_inputs(c)
+        spans, R0, r = c["spans"], c["R0"], c["r"]
+        N, d = q.shape[1], q.shape[2]
+        s = 1.0 / math.sqrt(d)
+        st = o.bound_statistics(q, k, spans, R0, r)
+        for h in range(c["H"]):
+            kk = k[h].tolist()
+            mu = [sum(kk[j][cc] for j in range(N)) / N for cc in range(d)]
+            cnorm = [math.sqrt(sum((kk[j][cc] - mu[cc]) ** 2 for cc in range(d))) for j in range(N)]
+            M = [max(cnorm[j] for j in range(N) if brute_frame(j, spans) == g) for g in range(len(spans))]
+            np.testing.assert_allclose(st["M"][h], M, rtol=1e-12, atol=1e-13)
+            for i in range(N):
+                f = brute_frame(i, spans)
+                keys = [j for j in range(N) if brute_sees(f, brute_frame(j, spans), R0, r)]
+                kbar = [sum(kk[j][cc] for j in keys) / len(keys) - mu[cc] for cc in range(d)]
+                qi = q[h, i].tolist()
+                b = s * math.sqrt(sum(x * x for x in qi)) * max(cnorm[j] for j in keys)
+                G = b - s * sum(qi[cc] * kbar[cc] for cc in range(d))
+                assert abs(st["b"][h, i] - b) < 1e-11
+                assert abs(st["G"][h, i] - G) < 1e-11
+        check_bound_holds(o, st=st, res=o.masked_attention(q, k, k, spans, R0, r))
+
+
+def check_ragged_equal_spans_reduce_to_uniform(o):
+    """A list of equal spans is the uniform geometry: same mask, same
+    attention, same bound statistics, and the closed-form pair count."""
+    rng = np.random.default_rng(45)
+    H, d, R0, F, T, r = 2, 8, 1, 6, 5, 1
+    N = (R0 + F) * T
+    q, k, v = (rng.standard_normal((H, N, d)) for _ in range(3))
+    spans = [T] * (R0 + F)
+    a = o.masked_attention(q, k, v, T, R0, r)
+    b = o.masked_attention(q, k, v, spans, R0, r)
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["lse"], b["lse"])
+    sa, sb = o.bound_statistics(q, k, T, R0, r), o.bound_statistics(q, k, spans, R0, r)
+    for name in ("M", "m", "G", "stat"):
+        np.testing.assert_allclose(sa[name], sb[name], rtol=1e-14, atol=1e-14)
+    assert o.visible_pairs(spans, F, R0, r) == closed_form_frame_pairs(F, R0, r) * T * T
+
+
+def check_ragged_block_sparse(o):
+    """Blocks of a size dividing every frame's span never straddle a frame:
+    an fp64 online-softmax loop over the visible frames' blocks gives the
+    dense masked result."""
+    for spans, R0, r, B in [([12, 4, 8, 16, 4, 8], 1, 1, 4), ([6, 9, 3, 12], 1, 0, 3)]:
+        rng = np.random.default_rng(46 + B)
+        H, d = 1, 8
+        N = sum(spans)
+        q, k, v = (rng.standard_normal((H, N, d)) for _ in range(3))
+        res = o.masked_attention(q, k, v, spans, R0, r)
+        s = 1.0 / math.sqrt(d)
+        starts = np.concatenate([[0], np.cumsum(spans)])
+        for f in range(len(spans)):
+            rows = np.arange(starts[f], starts[f + 1])
+            m, l, acc = np.full(len(rows), -np.inf), np.zeros(len(rows)), np.zeros((len(rows), d))
+            for g in range(len(spans)):
+                if not brute_sees(f, g, R0, r):
+                    continue
+                for b0 in range(starts[g], starts[g + 1], B):
+                    z = s * q[0, rows] @ k[0, b0:b0 + B].T
+                    m_new = np.maximum(m, z.max(axis=1))
+                    alpha = np.exp(m - m_new)
+                    p = np.exp(z - m_new[:, None])
+                    l = alpha * l + p.sum(axis=1)
+                    acc = alpha[:, None] * acc + p @ v[0, b0:b0 + B]
+                    m = m_new
+            np.testing.assert_allclose(acc / l[:, None], res["out"][0, rows], rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(m + np.log(l), res["lse"][0, rows], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # The pins.
 # ---------------------------------------------------------------------------
 
 CHECKS = [check_golden_frame_visibility, check_pair_counts, check_token_mask, check_attention_brute,
           check_full_window_is_sdpa, check_centring_invariance, check_q_zero_closed_form, check_invariants,
-          check_block_sparse, check_two_pass_merge, check_bound_stats_brute, check_bound_on_inputs]
+          check_block_sparse, check_two_pass_merge, check_bound_stats_brute, check_bound_on_inputs,
+          check_ragged_token_mask, check_ragged_attention_brute, check_ragged_bound_stats_brute,
+          check_ragged_equal_spans_reduce_to_uniform, check_ragged_block_sparse]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
@@ -492,3 +637,22 @@ def test_planted_uncentred_key_norms(monkeypatch):
 
     monkeypatch.setattr(ref, "bound_statistics", bad)
     assert _fails(check_bound_stats_brute)
+
+
+def test_planted_ragged_spans_taken_as_uniform(monkeypatch):
+    """A ragged oracle that treats every frame as having the first frame's
+    span (a plausible slip) fails the ragged pins."""
+    orig = ref.frame_spans
+
+    def bad(frame_tokens, n_tokens):
+        spans = orig(frame_tokens, n_tokens)
+        if len(spans) > 1 and not np.all(spans == spans[0]):
+            t0 = int(spans[0])
+            spans = np.full(len(spans), t0, dtype=np.int64)
+            spans[-1] = n_tokens - t0 * (len(spans) - 1)
+        return spans
+
+    monkeypatch.setattr(ref, "frame_spans", bad)
+    assert _fails(check_ragged_token_mask)
+    assert _fails(check_ragged_attention_brute)
+    assert _fails(check_ragged_bound_stats_brute)
