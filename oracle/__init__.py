@@ -44,3 +44,10 @@ from .reference import (  # noqa: F401
     frame_spans,
     frame_of,
 )
+from .prologue import (  # noqa: F401
+    RMS_EPS,
+    rms_norm,
+    rotate,
+    qkv_prologue,
+    prologue_flops,
+)

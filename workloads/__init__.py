@@ -176,3 +176,67 @@ def generate(w: Workload | str,
             list(ex.map(run, jobs))
     out["modified_heads"] = modified_heads(w)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Inputs of the attention prologue (normalization, projection, rotary
+# embedding, head packing): hidden states, norm scale, projection weight and
+# the rotary angle tables a caller supplies.  Random draws and position
+# tables only; the prologue's arithmetic is the oracle's and the library's.
+# ---------------------------------------------------------------------------
+
+#: Latent grid width (patches per row) of each workload's frames: the frame
+#: span T is grid_w x (T / grid_w) patches.
+GRID_W = {"tiny": 8, "mid": 40, "720p": 80, "1080p": 120, "stress": 80, "dense": 80, "720p_h4": 80}
+
+
+def rotary_tables(w: Workload, grid_w: Optional[int] = None, base: float = 10000.0):
+    """cos, sin [N, d/2] float32 for 3D rotary positions (frame, row, column).
+
+    Token j of frame f = j // T sits at row (j % T) // grid_w and column
+    (j % T) % grid_w.  The d/2 rotation pairs are split over the three axes
+    (d/8 pairs for the frame index, the rest shared equally by row and
+    column); pair k of an axis with n pairs turns at base^(-k/n) radians per
+    unit of that axis's position.
+    """
+    d = w.head_dim
+    gw = grid_w or GRID_W.get(w.name, 1)
+    n_t = d // 8
+    n_y = (d // 2 - n_t) // 2
+    n_x = d // 2 - n_t - n_y
+    j = np.arange(w.tokens, dtype=np.int64)
+    pos = [j // w.frame_tokens, (j % w.frame_tokens) // gw, (j % w.frame_tokens) % gw]
+    angles = [p[:, None].astype(np.float64) * base ** (-np.arange(n, dtype=np.float64) / n)[None, :]
+              for p, n in zip(pos, (n_t, n_y, n_x))]
+    ang = np.concatenate(angles, axis=1)
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def prologue_inputs(w: Workload | str, width: Optional[int] = None, workers: Optional[int] = None):
+    """Hidden states x [N, C] (bf16 bits, N(0,1)), norm scale gamma [C]
+    (float32, 1 + 0.1 N(0,1)), projection weight [3*H*d, C] (bf16 bits,
+    N(0, 1/C)) and the rotary tables; C defaults to H*d.  Streams:
+    (seed, 10, row block) for x, (seed, 11) gamma, (seed, 12, row block)
+    for the weight."""
+    if isinstance(w, str):
+        w = get(w)
+    C = width or w.heads * w.head_dim
+    out_f = 3 * w.heads * w.head_dim
+    x = np.empty((w.tokens, C), dtype=np.uint16)
+    wt = np.empty((out_f, C), dtype=np.uint16)
+    rows = 4096
+    jobs = [(x, i, 10, 1.0) for i in range(0, w.tokens, rows)] + \
+           [(wt, i, 12, 1.0 / np.sqrt(C)) for i in range(0, out_f, rows)]
+
+    def run(job):
+        arr, i0, tag, scale = job
+        n = min(rows, arr.shape[0] - i0)
+        vals = _stream(w.seed, tag, i0 // rows).standard_normal((n, C), dtype=np.float32)
+        arr[i0:i0 + n] = round_to_bf16_bits(vals * np.float32(scale))
+
+    nw = workers or min(len(jobs), os.cpu_count() or 1, 16)
+    with ThreadPoolExecutor(max_workers=nw) as ex:
+        list(ex.map(run, jobs))
+    gamma = (1.0 + 0.1 * _stream(w.seed, 11).standard_normal(C)).astype(np.float32)
+    cos, sin = rotary_tables(w)
+    return {"x": x, "gamma": gamma, "w": wt, "cos": cos, "sin": sin}
