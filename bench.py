@@ -15,6 +15,8 @@ Arms:
   python bench.py [--gpus N] [--steps K] [--warmup W]     this library
   python bench.py --impl reference ...                      the fp64 oracle on
       the host cores, a bounded sample of the same workload per step
+  python bench.py --impl ablation ...                       the splash-style
+      two-pass kernel ("Deleting the Mask": the "before") on the same step
 
 Prints one JSON line (rank 0).
 """
@@ -70,6 +72,12 @@ def job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> floa
     scaling), so the job does world * steps chunks in the slowest rank's
     time."""
     return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
+def prepass_algorithmic_bytes(H: int, N: int, d: int) -> int:
+    """The prepass reads K and Q once (bf16) and writes one fp32 bound per
+    row; the per-head statistics are a few hundred KB more and not counted."""
+    return 2 * H * N * d * 2 + H * N * 4
 
 
 def visible_flops(w) -> float:
@@ -143,27 +151,38 @@ def l2_note(qkv_bytes: int) -> str:
     return f"inputs ({qkv_bytes / 1e6:.1f} MB Q/K/V) fit in L2: L2-resident timing"
 
 
-def kernel_fingerprint() -> str:
+KERNEL_SOURCES = {
+    "attention_fwd": ("attention.cu", "ptx.cuh", "kernels.h", "internal.h"),
+    "prepass_kernel": ("prepass.cu", "kernels.h", "internal.h"),
+}
+
+
+def kernel_fingerprint(kernel: str = "attention_fwd") -> str:
+    """Hash of the sources a kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "frame_aligned_sparse_gb300", "csrc")
-    for name in ("attention.cu", "ptx.cuh", "kernels.h", "internal.h"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "attention_fwd_720p.md")
-    if not os.path.exists(path):
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum
+    from one ncu capture) of a kernel on a workload, from the data file
+    beside the ncu summaries; only while the kernel's sources still hash to
+    the fingerprint recorded with the figure."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
-    fp = kernel_fingerprint()
-    for line in open(path):
-        if line.startswith("traffic_per_launch_bytes:"):
-            parts = line.split()
-            if len(parts) >= 4 and parts[3] == fp:
-                return float(parts[1])
+    fp = kernel_fingerprint(kernel)
+    for line in open(TRAFFIC_FILE):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+            if parts[3] == fp:
+                return float(parts[2])
     return None
 
 
@@ -287,26 +306,37 @@ def run_fas(args, w):
 
     launches = [0]
 
+    ablation = args.impl == "ablation"
+
     def step(ev=None):
         plan()
-        fas.fas_prepass(q, k, stream=stream)
-        launches[0] += fas.fas_last_launch_count()
         if ev is not None:
             ev[0].record(stream)
-        fas.fas_forward(q, k, v, out, lse, mode=args.mode, stream=stream)
-        launches[0] += fas.fas_last_launch_count()
+        if not ablation:
+            fas.fas_prepass(q, k, stream=stream)
+            launches[0] += fas.fas_last_launch_count()
         if ev is not None:
             ev[1].record(stream)
+        if ablation:
+            # The splash-style "before": padded 128-multiple tiles, mask
+            # predicates, window and reference passes, merge.
+            fas.fas_forward_ablation(q, k, v, out, lse, stream=stream)
+        else:
+            fas.fas_forward(q, k, v, out, lse, mode=args.mode, stream=stream)
+        launches[0] += fas.fas_last_launch_count()
+        if ev is not None:
+            ev[2].record(stream)
 
     for _ in range(args.warmup):
         step()
     if fas.fas_status(stream) != 0:
         raise RuntimeError("device-side wait timed out during warm-up")
     elig = fas.fas_prepass(q, k, stream=stream, want_elig=True)
+    if ablation:
+        step()
 
     sampler = ClockSampler(local)
-    fwd_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
+    step_events = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -316,7 +346,7 @@ def run_fas(args, w):
     launches[0] = 0
     t_start.record(stream)
     for i in range(args.steps):
-        step(fwd_events[i])
+        step(step_events[i])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
@@ -326,12 +356,13 @@ def run_fas(args, w):
         raise RuntimeError("device-side wait timed out in the timed region")
     timed_launches = launches[0]
     ms_total = t_start.elapsed_time(t_end)
-    fwd_ms = [a.elapsed_time(b) for a, b in fwd_events]
+    pre_ms = [a.elapsed_time(b) for a, b, _ in step_events]
+    fwd_ms = [b.elapsed_time(c) for _, b, c in step_events]
     ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     value = job_tflops(world, flops, args.steps, ms_total)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    prepass_ms = ms_step - fwd_avg
+    prepass_ms = sum(pre_ms) / len(pre_ms)
 
     # End to end through the public API: pinned host inputs in, host results
     # out (fas_forward_host), every copy inside the timed region.
@@ -364,13 +395,72 @@ def run_fas(args, w):
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
     achieved = flops / (fwd_avg * 1e-3) / 1e12
+    pre_bytes = prepass_algorithmic_bytes(H, N, d)
+    sm_mhz = (clocks or {}).get("sm_mhz")
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f_, s_, n_ = oracle_sample(w, x, tile_order(w, seed=1), budget_s=args.cpu_budget)
         cpu = {"value": f_ / s_ / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{n_} random query tiles (128 rows, one head each) of the {w.name} workload, "
                          f"fp64 dense masked attention over all {w.tokens} keys, {s_:.1f} s"}
+
+    pro = None
+    if not ablation and not args.no_prologue:
+        # The prologue on the same geometry: hidden states [N, H*d] -> q, k, v
+        # in the step's layout (RMSNorm, projection on the tensor cores,
+        # rotary, head packing), then the step's prepass and attention on
+        # its outputs.
+        pin_ = workloads.prologue_inputs(w)
+        px = torch.from_numpy(pin_["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+        pw = torch.from_numpy(pin_["w"].view(np.int16)).view(torch.bfloat16).to(dev)
+        pg, pc, ps = (torch.from_numpy(pin_[t]).to(dev) for t in ("gamma", "cos", "sin"))
+        wf = fas.fas_prologue_fold_weights(pw, pg, stream=stream)
+        qkv = fas.fas_prologue(px, wf, pc, ps, H, d, layout=args.layout, stream=stream)
+        n_pro = 5
+        pe = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(n_pro)]
+        for i in range(n_pro + 2):
+            ev = pe[i - 2] if i >= 2 else None
+            if ev is not None:
+                ev[0].record(stream)
+            fas.fas_prologue(px, wf, pc, ps, H, d, layout=args.layout, q=qkv[0], k=qkv[1], v=qkv[2], stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            fas.fas_prepass(qkv[0], qkv[1], stream=stream)
+            fas.fas_forward(qkv[0], qkv[1], qkv[2], out, lse, mode=args.mode, stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+        torch.cuda.synchronize(dev)
+        pro_ms = sum(a.elapsed_time(b) for a, b, _ in pe) / n_pro
+        chain_ms = sum(a.elapsed_time(c) for a, _, c in pe) / n_pro
+        pflops = 2.0 * N * (H * d) * 3 * H * d
+        pro = {"kernel": "prologue_qkv", "bound": "tensor", "ms": pro_ms,
+               "achieved": pflops / (pro_ms * 1e-3) / 1e12, "peak": peak, "unit": "TFLOP/s",
+               "frac": pflops / (pro_ms * 1e-3) / 1e12 / peak, "flops": pflops,
+               "shape": f"x [{N}, {H * d}] -> q, k, v ({args.layout}), projection {H * d} -> {3 * H * d}",
+               "step_with_prologue_ms": chain_ms, "launches_timed": n_pro}
+        del px, pw, wf, qkv
+
+    abl = None
+    if not ablation and not args.no_ablation and args.layout == "hnd":
+        # The splash-style ablation on the same inputs, timed the same way,
+        # for the "before" beside the frame-aligned kernel's time.
+        out_a, lse_a = torch.empty_like(out), torch.empty_like(lse)
+        for _ in range(2):
+            fas.fas_forward_ablation(q, k, v, out_a, lse_a, stream=stream)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_abl = 5
+        a0.record(stream)
+        for _ in range(n_abl):
+            fas.fas_forward_ablation(q, k, v, out_a, lse_a, stream=stream)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        abl_ms = a0.elapsed_time(a1) / n_abl
+        abl = {"kernels": "ablation_fwd (window pass, reference pass) + ablation_merge", "ms": abl_ms,
+               "tflops": flops / (abl_ms * 1e-3) / 1e12, "frac": flops / (abl_ms * 1e-3) / 1e12 / peak,
+               "frame_aligned_speedup": abl_ms / fwd_avg, "launches_timed": n_abl}
+        del out_a, lse_a
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -386,18 +476,32 @@ def run_fas(args, w):
         },
         "ms_per_chunk": fwd_avg,
         "pct_bf16_peak": 100.0 * achieved / peak,
-        "prepass": {"ms": prepass_ms, "gbs": 3 * H * N * d * 2 / (prepass_ms * 1e-3) / 1e9,
-                    "bytes": "K read twice + Q read once"},
+        "prepass": {"kernel": "prepass_kernel", "ms": prepass_ms, "bound": "hbm",
+                    "achieved": pre_bytes / (prepass_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                    "frac": pre_bytes / (prepass_ms * 1e-3) / 1e9 / hbm, "peak_source": f"hbm_gbs ({peak_src})",
+                    "algorithmic_bytes": pre_bytes,
+                    "bytes": "one read of K and of Q (bf16) plus the fp32 row bounds written",
+                    "traffic": recorded_traffic("prepass_kernel", w.name)},
         "roofline": {"bound": "tensor", "kernel": "attention_fwd", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"bf16_tflops ({peak_src})",
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
-                     "traffic": recorded_traffic()},
+                     "sm_mhz_median": sm_mhz,
+                     "tflop_per_sm_ghz": achieved / (sm_mhz / 1e3) if sm_mhz else None,
+                     "traffic": recorded_traffic("attention_fwd", w.name)},
         "cpu_baseline": cpu,
         "e2e": {"value": job_tflops(world, flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": timed_launches,
         "clocks": clocks,
+        "ablation": abl,
+        "prologue": pro,
     }
+    if ablation:
+        line["impl"] = "ablation"
+        line["roofline"]["kernel"] = "ablation_fwd + ablation_merge"
+        line["roofline"]["traffic"] = None
+        line.pop("prepass")
+        line["e2e"] = None  # the host-buffer entry point runs the frame-aligned kernel, not the ablation
     if rank == 0:
         print(json.dumps(line), flush=True)
     fas.fas_free()
@@ -411,7 +515,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=["fas", "reference"], default="fas")
+    ap.add_argument("--impl", choices=["fas", "reference", "ablation"], default="fas",
+                    help="fas: this library; reference: the fp64 oracle on the host cores; ablation: the "
+                         "splash-style two-pass kernel in place of the frame-aligned one")
     ap.add_argument("--workload", default="720p", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--mode", default="auto", choices=["auto", "online", "bounded"])
     ap.add_argument("--block-k", type=int, default=0)
@@ -419,6 +525,8 @@ def main():
                     help="q, k, v, out as [H, N, d] or token-major [N, H, d]")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true", help="skip timing the splash-style ablation")
+    ap.add_argument("--no-prologue", action="store_true", help="skip timing the fused prologue")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     w = workloads.get(args.workload)

@@ -24,7 +24,8 @@ __all__ = [
     "FasError", "PlanInfo", "MODES", "library_path", "load",
     "fas_plan", "fas_plan_describe", "fas_prepass", "fas_forward", "fas_free",
     "fas_status", "fas_prepass_readback", "fas_selftest_wait_timeout", "fas_last_launch_count",
-    "fas_prepass_noalloc", "fas_forward_host", "fas_set_layout", "LAYOUTS",
+    "fas_prepass_noalloc", "fas_forward_host", "fas_set_layout", "LAYOUTS", "fas_forward_ablation",
+    "fas_prologue", "fas_prologue_fold_weights", "PROLOGUE_LAYOUTS",
 ]
 
 FAS_OK, FAS_ERR_ARG, FAS_ERR_STATE, FAS_ERR_ALIGN, FAS_ERR_CUDA, FAS_ERR_TIMEOUT, FAS_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
@@ -32,6 +33,8 @@ FAS_ERR_SCRATCH = -7
 FAS_NOALLOC_SCRATCH_BYTES = 4 << 20
 MODES = {"auto": 0, "online": 1, "bounded": 2}
 LAYOUTS = {"hnd": 0, "nhd": 1}  # q, k, v, out as [H, N, d] or [N, H, d]
+PROLOGUE_LAYOUTS = {"hnd": 0, "nhd": 1, "a2a": 2}  # fas_prologue's outputs (a2a: [G, P, n, H/(G*P), d])
+RMS_EPS = 1e-6
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -78,9 +81,16 @@ _SIGS = {
     "fas_plan_ex": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(_PlanInfoC)]),
     "fas_plan_describe": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.POINTER(_PlanInfoC), ctypes.c_void_p,
                                                               ctypes.c_void_p]),
+    "fas_plan_ragged": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_int] * 6 + [ctypes.POINTER(_PlanInfoC)]),
+    "fas_plan_describe_ragged": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_int] * 6 +
+                                 [ctypes.POINTER(_PlanInfoC), ctypes.c_void_p, ctypes.c_void_p]),
     "fas_prepass": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "fas_forward": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_void_p]),
     "fas_forward_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "fas_forward_ablation": (ctypes.c_int, [ctypes.c_void_p] * 6),
+    "fas_prologue": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 + [ctypes.c_float] +
+                     [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]),
+    "fas_prologue_fold_weights": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p]),
     "fas_free": (ctypes.c_int, []),
     "fas_status": (ctypes.c_int, [ctypes.c_void_p]),
     "fas_prepass_readback": (ctypes.c_int, [ctypes.c_void_p] * 6),
@@ -133,15 +143,33 @@ def _info(c: _PlanInfoC, table: Optional[np.ndarray] = None) -> PlanInfo:
 _PLAN: dict = {}
 
 
-def fas_plan(frame_tokens: int, n_frames: int, ref_frames: int, window_radius: int, heads: int, head_dim: int,
+def _spans_arg(frame_tokens, n_frames: int, ref_frames: int):
+    """(int32 array of per-frame spans, or None for uniform frames)."""
+    if np.ndim(frame_tokens) == 0:
+        return None
+    spans = np.ascontiguousarray(frame_tokens, dtype=np.int32)
+    if spans.ndim != 1 or len(spans) != ref_frames + n_frames:
+        raise ValueError(f"frame_tokens must hold ref_frames + n_frames = {ref_frames + n_frames} spans")
+    return spans
+
+
+def fas_plan(frame_tokens, n_frames: int, ref_frames: int, window_radius: int, heads: int, head_dim: int,
              block_k: int = 0) -> PlanInfo:
-    """Builds (or reuses) the library's plan; see ``fas_plan`` in fas.h."""
+    """Builds (or reuses) the library's plan; see ``fas_plan`` in fas.h.
+    ``frame_tokens``: one span for every frame, or a sequence of
+    ref_frames + n_frames per-frame spans (``fas_plan_ragged``)."""
     c = _PlanInfoC()
-    rc = load().fas_plan_ex(frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k,
-                            ctypes.byref(c))
+    spans = _spans_arg(frame_tokens, n_frames, ref_frames)
+    if spans is None:
+        rc = load().fas_plan_ex(frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k,
+                                ctypes.byref(c))
+    else:
+        rc = load().fas_plan_ragged(spans.ctypes.data, n_frames, ref_frames, window_radius, heads, head_dim,
+                                    block_k, ctypes.byref(c))
     _check("fas_plan", rc)
     info = _info(c)
-    geometry = (frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, info.block_k)
+    geometry = (tuple(spans.tolist()) if spans is not None else frame_tokens, n_frames, ref_frames, window_radius,
+                heads, head_dim, info.block_k)
     if _PLAN.get("geometry") != geometry:
         _PLAN["layout"] = "hnd"  # a new plan starts head-major (the library resets it too)
     _PLAN.update(heads=heads, head_dim=head_dim, tokens=info.tokens, info=info, geometry=geometry)
@@ -155,18 +183,25 @@ def fas_set_layout(layout: str) -> None:
     _PLAN["layout"] = layout
 
 
-def fas_plan_describe(frame_tokens: int, n_frames: int, ref_frames: int, window_radius: int, heads: int,
+def fas_plan_describe(frame_tokens, n_frames: int, ref_frames: int, window_radius: int, heads: int,
                       head_dim: int, block_k: int = 0) -> Tuple[PlanInfo, np.ndarray, np.ndarray]:
-    """Host-only plan: (info, table [Nf, 4], work [n_work, 4])."""
+    """Host-only plan: (info, table [Nf, 4], work [n_work, 4]).  frame_tokens
+    as in ``fas_plan``."""
     lib = load()
+    spans = _spans_arg(frame_tokens, n_frames, ref_frames)
+
+    def call(c, table, work):
+        if spans is None:
+            return lib.fas_plan_describe(frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim,
+                                         block_k, ctypes.byref(c), table, work)
+        return lib.fas_plan_describe_ragged(spans.ctypes.data, n_frames, ref_frames, window_radius, heads,
+                                            head_dim, block_k, ctypes.byref(c), table, work)
+
     c = _PlanInfoC()
-    _check("fas_plan_describe", lib.fas_plan_describe(frame_tokens, n_frames, ref_frames, window_radius, heads,
-                                                      head_dim, block_k, ctypes.byref(c), None, None))
+    _check("fas_plan_describe", call(c, None, None))
     table = np.zeros((c.total_frames, 4), dtype=np.int32)
     work = np.zeros((c.n_work, 4), dtype=np.int32)
-    _check("fas_plan_describe", lib.fas_plan_describe(frame_tokens, n_frames, ref_frames, window_radius, heads,
-                                                      head_dim, block_k, ctypes.byref(c),
-                                                      table.ctypes.data, work.ctypes.data))
+    _check("fas_plan_describe", call(c, table.ctypes.data, work.ctypes.data))
     return _info(c, table), table, work
 
 
@@ -224,6 +259,77 @@ def fas_forward(q, k, v, out=None, lse=None, mode: str = "auto", stream=None):
                             MODES[mode], _stream_handle(stream))
     _check("fas_forward", rc)
     return out, lse
+
+
+def fas_forward_ablation(q, k, v, out=None, lse=None, stream=None):
+    """The splash-style ablation (128-multiple tiles, padding, mask
+    predicates, two passes and a merge; see ``fas_forward_ablation`` in
+    fas.h); head-major [H, N, d] only.  Returns (out, lse)."""
+    import torch
+    shape = _qkv_shape()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(name, t, shape, torch.bfloat16)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(_lse_shape(), dtype=torch.float32, device=q.device)
+    _check_tensor("out", out, shape, torch.bfloat16)
+    _check_tensor("lse", lse, _lse_shape(), torch.float32)
+    rc = load().fas_forward_ablation(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                     _stream_handle(stream))
+    _check("fas_forward_ablation", rc)
+    return out, lse
+
+
+def fas_prologue_fold_weights(w, gamma, out=None, stream=None):
+    """W' = bf16(W * gamma) per input feature (see fas.h): w bf16
+    [3*H*d, C], gamma fp32 [C] (CUDA tensors)."""
+    import torch
+    O, C = w.shape
+    _check_tensor("w", w, (O, C), torch.bfloat16)
+    _check_tensor("gamma", gamma, (C,), torch.float32)
+    if out is None:
+        out = torch.empty_like(w)
+    _check_tensor("out", out, (O, C), torch.bfloat16)
+    _check("fas_prologue_fold_weights",
+           load().fas_prologue_fold_weights(w.data_ptr(), gamma.data_ptr(), out.data_ptr(), C, O,
+                                            _stream_handle(stream)))
+    return out
+
+
+def fas_prologue(x, w_folded, cos, sin, heads: int, head_dim: int, layout: str = "hnd", groups: int = 1,
+                 ranks: int = 1, q=None, k=None, v=None, eps: float = RMS_EPS, stream=None):
+    """RMSNorm -> QKV projection -> rotary -> head packing in one kernel
+    (see ``fas_prologue`` in fas.h).  x bf16 [N, C]; w_folded bf16
+    [3*H*d, C]; cos, sin fp32 [N, d/2].  Returns (q, k, v) bf16 in
+    ``layout``: "hnd" [H, N, d], "nhd" [N, H, d] or "a2a" [G, P, N, H/(G*P), d]."""
+    import torch
+    N, C = x.shape
+    _check_tensor("x", x, (N, C), torch.bfloat16)
+    _check_tensor("w_folded", w_folded, (3 * heads * head_dim, C), torch.bfloat16)
+    _check_tensor("cos", cos, (N, head_dim // 2), torch.float32)
+    _check_tensor("sin", sin, (N, head_dim // 2), torch.float32)
+    if layout == "hnd":
+        shape = (heads, N, head_dim)
+    elif layout == "nhd":
+        shape = (N, heads, head_dim)
+    elif layout == "a2a":
+        if heads % (groups * ranks):
+            raise ValueError(f"heads ({heads}) must divide into {groups} groups x {ranks} ranks")
+        shape = (groups, ranks, N, heads // (groups * ranks), head_dim)
+    else:
+        raise ValueError(layout)
+    outs = []
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t is None:
+            t = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
+        _check_tensor(name, t, shape, torch.bfloat16)
+        outs.append(t)
+    rc = load().fas_prologue(x.data_ptr(), w_folded.data_ptr(), cos.data_ptr(), sin.data_ptr(), N, C, heads,
+                             head_dim, float(eps), outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
+                             PROLOGUE_LAYOUTS[layout], groups, ranks, _stream_handle(stream))
+    _check("fas_prologue", rc)
+    return tuple(outs)
 
 
 def _check_host_tensor(name, t, shape, dtype):
@@ -300,6 +406,11 @@ def fas_prepass_noalloc(q, k, frame_tokens: int, n_frames: int, ref_frames: int,
     stat: fp32 [H]; elig: uint8 [H] (all CUDA tensors)."""
     import torch
     H, N, d = q.shape
+    if N != (ref_frames + n_frames) * frame_tokens:
+        # The C call has no plan to check the buffers against: a geometry
+        # that does not match q would read past the ends of q and k.
+        raise ValueError(f"q has {N} rows per head; the geometry needs (ref_frames + n_frames) * frame_tokens = "
+                         f"{(ref_frames + n_frames) * frame_tokens}")
     _check_tensor("q", q, (H, N, d), torch.bfloat16)
     _check_tensor("k", k, (H, N, d), torch.bfloat16)
     _check_tensor("row_bound", row_bound, (H, N), torch.float32)

@@ -8,6 +8,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "fas.h"
@@ -25,17 +26,20 @@ struct State {
   void* arena = nullptr;
   int4* work = nullptr;
   int4* table = nullptr;
-  float* partial = nullptr;
+  int2* spans = nullptr;
+  int4* fvis = nullptr;
+  float* ksum_part = nullptr;
   float* mu = nullptr;
   float* fsum = nullptr;
-  float* mpart = nullptr;
+  float* kmax_part = nullptr;
   float* frame_max = nullptr;
   float* mvis = nullptr;
   float* kbarc = nullptr;
   float* row_bound = nullptr;
-  float* gpart = nullptr;
+  float* gmax_part = nullptr;
   float* stat = nullptr;
   uint8_t* elig = nullptr;
+  unsigned int* sync = nullptr;
   unsigned int* err = nullptr;
   const void* pre_q = nullptr;
   const void* pre_k = nullptr;
@@ -56,6 +60,12 @@ struct State {
   std::vector<cudaEvent_t> ev_in, ev_done;
   cudaEvent_t ev_entry = nullptr, ev_exit = nullptr;
   bool exit_recorded = false;
+  // fas_forward_ablation: both passes' work lists and fp32 intermediates.
+  void* abl = nullptr;
+  int4* abl_work[2] = {nullptr, nullptr};
+  int abl_items[2] = {0, 0};
+  float *abl_o[2] = {nullptr, nullptr}, *abl_lse[2] = {nullptr, nullptr};
+  int64_t abl_npad = 0;
 };
 
 State g_state;
@@ -102,7 +112,7 @@ void fill_info(const HostPlan& p, fas_plan_info* info) {
 
 void release() {
   State& s = g_state;
-  if (s.arena || s.io || s.st_h2d) {
+  if (s.arena || s.io || s.st_h2d || s.abl) {
     int cur = -1;
     cudaGetDevice(&cur);
     if (s.device >= 0 && cur != s.device) cudaSetDevice(s.device);
@@ -115,6 +125,7 @@ void release() {
     for (cudaEvent_t e : {s.ev_entry, s.ev_exit})
       if (e) cudaEventDestroy(e);
     if (s.gwork) cudaFree(s.gwork);
+    if (s.abl) cudaFree(s.abl);
     if (s.io) cudaFree(s.io);
     if (s.arena) cudaFree(s.arena);
     if (cur >= 0 && cur != s.device) cudaSetDevice(cur);
@@ -133,17 +144,20 @@ int allocate(const HostPlan& p) {
   Part parts[] = {
       {(size_t)p.n_work * sizeof(int4), (void**)&s.work},
       {Nf * sizeof(int4), (void**)&s.table},
-      {H * Nf * C * D * 4, (void**)&s.partial},
+      {Nf * sizeof(int2), (void**)&s.spans},
+      {Nf * sizeof(int4), (void**)&s.fvis},
+      {H * Nf * C * D * 4, (void**)&s.ksum_part},
       {H * D * 4, (void**)&s.mu},
       {H * Nf * D * 4, (void**)&s.fsum},
-      {H * Nf * C * 4, (void**)&s.mpart},
+      {H * Nf * C * 4, (void**)&s.kmax_part},
       {H * Nf * 4, (void**)&s.frame_max},
       {H * Nf * 4, (void**)&s.mvis},
       {H * Nf * D * 4, (void**)&s.kbarc},
       {H * N * 4, (void**)&s.row_bound},
-      {H * Nf * C * 4, (void**)&s.gpart},
+      {H * Nf * C * 4, (void**)&s.gmax_part},
       {H * 4, (void**)&s.stat},
       {H, (void**)&s.elig},
+      {fas::prepass_sync_words(p.H, p.Nf) * 4, (void**)&s.sync},
       {sizeof(unsigned int), (void**)&s.err},
   };
   size_t total = 0;
@@ -160,6 +174,10 @@ int allocate(const HostPlan& p) {
   if (cudaMemcpy(s.work, p.work.data(), p.work.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
     return FAS_ERR_CUDA;
   if (cudaMemcpy(s.table, p.table.data(), p.table.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+    return FAS_ERR_CUDA;
+  if (cudaMemcpy(s.spans, p.spans.data(), p.spans.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+    return FAS_ERR_CUDA;
+  if (cudaMemcpy(s.fvis, p.fvis.data(), p.fvis.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
     return FAS_ERR_CUDA;
   return FAS_OK;
 }
@@ -208,18 +226,23 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   a.k = static_cast<const uint16_t*>(k) + h0 * head_stride();
   a.row_stride = row_stride();
   a.head_stride = head_stride();
-  a.table = s.table;
-  a.partial = s.partial + H0 * Nf * C * D;
+  a.spans = s.spans;
+  a.fvis = s.fvis;
+  a.R0 = p.R0;
+  a.r = p.r;
+  a.ksum_part = s.ksum_part + H0 * Nf * C * D;
+  a.kmax_part = s.kmax_part + H0 * Nf * C;
+  a.gmax_part = s.gmax_part + H0 * Nf * C;
   a.mu = s.mu + H0 * D;
   a.fsum = s.fsum + H0 * Nf * D;
-  a.mpart = s.mpart + H0 * Nf * C;
   a.frame_max = s.frame_max + H0 * Nf;
   a.mvis = s.mvis + H0 * Nf;
   a.kbarc = s.kbarc + H0 * Nf * D;
   a.row_bound = s.row_bound + H0 * N;
-  a.gpart = s.gpart + H0 * Nf * C;
   a.stat = s.stat + H0;
   a.elig = s.elig + H0;
+  a.sync = s.sync;  // one launch at a time: the calls that launch the prepass serialise on one stream
+  a.err = s.err;
   a.N = p.N;
   a.T = p.T;
   a.Nf = p.Nf;
@@ -227,23 +250,29 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   a.d = p.d;
   a.chunks = p.chunks;
   a.scale = (float)(1.0 / sqrt((double)p.d));
+  a.limit_ns = fas::kWaitLimitNs;
   return a;
 }
 
-// Tensor maps of q, k, v (device bf16 [H, N, d]).  Q is [H][Nf][T][d] so a
-// tile's rows past the frame end read as zeros.
+// Tensor maps of q, k, v (device bf16, current layout).  With uniform frames
+// Q is [H][Nf][T][d], so a tile's rows past the frame end read as zeros;
+// with ragged frames Q is [H][N][d] and a tile's rows past the frame end
+// are the next frame's (computed, never stored).
 int encode_qkv(const void* q, const void* k, const void* v, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
   const HostPlan& p = g_state.plan;
   const cuuint64_t D = (cuuint64_t)p.d;
   const cuuint64_t rs = (cuuint64_t)row_stride() * 2, hs = (cuuint64_t)head_stride() * 2;  // bytes
-  {
-    const cuuint64_t dims[4] = {D, (cuuint64_t)p.T, (cuuint64_t)p.Nf, (cuuint64_t)p.H};
-    const cuuint64_t strides[3] = {rs, (cuuint64_t)p.T * rs, hs};
-    const cuuint32_t box[4] = {64, (cuuint32_t)fas::kQTile, 1, 1};
-    if (encode(tq, q, 4, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
-  }
   const cuuint64_t dims[3] = {D, (cuuint64_t)p.N, (cuuint64_t)p.H};
   const cuuint64_t strides[2] = {rs, hs};
+  if (!p.ragged) {
+    const cuuint64_t qdims[4] = {D, (cuuint64_t)p.T, (cuuint64_t)p.Nf, (cuuint64_t)p.H};
+    const cuuint64_t qstrides[3] = {rs, (cuuint64_t)p.T * rs, hs};
+    const cuuint32_t box[4] = {64, (cuuint32_t)fas::kQTile, 1, 1};
+    if (encode(tq, q, 4, qdims, qstrides, box) != FAS_OK) return FAS_ERR_CUDA;
+  } else {
+    const cuuint32_t box[3] = {64, (cuuint32_t)fas::kQTile, 1};
+    if (encode(tq, q, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
+  }
   const cuuint32_t box[3] = {64, (cuuint32_t)p.Bk, 1};
   if (encode(tk, k, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
   if (encode(tv, v, 3, dims, strides, box) != FAS_OK) return FAS_ERR_CUDA;
@@ -258,6 +287,8 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   fas::FwdParams fp;
   fp.work = work;
   fp.table = s.table;
+  fp.spans = s.spans;
+  fp.q_by_frame = p.ragged ? 0 : 1;
   fp.row_bound = s.row_bound;
   fp.elig = s.elig;
   fp.out = static_cast<uint16_t*>(out);
@@ -266,7 +297,6 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   fp.lse = lse;
   fp.err = s.err;
   fp.N = p.N;
-  fp.T = p.T;
   fp.Bk = p.Bk;
   fp.mode = mode;
   fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.d));
@@ -344,21 +374,12 @@ int ensure_host_pipeline(int hg) {
   return FAS_OK;
 }
 
-int check_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FAS_ERR_CUDA;
-  if (g_state.planned && dev != g_state.device) return FAS_ERR_STATE;
-  return FAS_OK;
-}
-
-}  // namespace
-
-extern "C" {
-
-int fas_plan_describe(int frame_tokens, int n_frames, int ref_frames, int window_radius, int heads, int head_dim,
-                      int block_k, fas_plan_info* info, int32_t* table, int32_t* work) {
+int describe(const int32_t* spans, int frame_tokens, int n_frames, int ref_frames, int window_radius, int heads,
+             int head_dim, int block_k, fas_plan_info* info, int32_t* table, int32_t* work) {
+  if (spans && (n_frames < 1 || ref_frames < 0)) return FAS_ERR_ARG;
   HostPlan p;
-  const int rc = fas::build_plan(frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k, &p);
+  const int rc =
+      fas::build_plan(spans, frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k, &p);
   if (rc != FAS_OK) return rc;
   if (info) {
     fill_info(p, info);
@@ -369,10 +390,11 @@ int fas_plan_describe(int frame_tokens, int n_frames, int ref_frames, int window
   return FAS_OK;
 }
 
-int fas_plan_ex(int frame_tokens, int n_frames, int ref_frames, int window_radius, int heads, int head_dim,
-                int block_k, fas_plan_info* info) {
+int make_plan(const int32_t* spans, int frame_tokens, int n_frames, int ref_frames, int window_radius, int heads,
+              int head_dim, int block_k, fas_plan_info* info) {
+  if (spans && (n_frames < 1 || ref_frames < 0)) return FAS_ERR_ARG;
   HostPlan p;
-  int rc = fas::build_plan(frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k, &p);
+  int rc = fas::build_plan(spans, frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k, &p);
   if (rc != FAS_OK) return rc;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FAS_ERR_CUDA;
@@ -394,9 +416,142 @@ int fas_plan_ex(int frame_tokens, int n_frames, int ref_frames, int window_radiu
   return FAS_OK;
 }
 
+// The ablation's work lists: per pass, one item per (head, 128-row query
+// tile of the padded sequence) with the tile's key range rounded out to
+// 128 tokens: the union of its rows' windows (pass 0) or the reference
+// frames (pass 1).  Heaviest items first.
+void ablation_work(const HostPlan& p, int pass, std::vector<int32_t>* out) {
+  const int64_t npad = (p.N + 127) / 128 * 128;
+  const int64_t T = p.T;
+  std::vector<int32_t> items;
+  for (int h = 0; h < p.H; ++h)
+    for (int64_t qt = 0; qt * 128 < npad; ++qt) {
+      const int64_t r0 = qt * 128, r1 = std::min<int64_t>(r0 + 128, p.N) - 1;  // valid rows of the tile
+      int64_t lo, hi;
+      if (pass == 1) {
+        lo = 0;
+        hi = (int64_t)p.R0 * T;
+      } else {
+        const int fa = (int)(r0 / T), fb = (int)(r1 / T);
+        if (fa < p.R0) {
+          lo = (int64_t)p.R0 * T;
+          hi = p.N;
+        } else {
+          lo = (int64_t)std::max(p.R0, fa - p.r) * T;
+          hi = (int64_t)(std::min(p.Nf - 1, fb + p.r) + 1) * T;
+        }
+      }
+      lo = lo / 128 * 128;
+      hi = (hi + 127) / 128 * 128;
+      if (hi <= lo) continue;
+      items.insert(items.end(), {h, (int32_t)qt, (int32_t)lo, (int32_t)((hi - lo) / 128)});
+    }
+  const size_t n = items.size() / 4;
+  std::vector<size_t> order(n);
+  for (size_t i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](size_t a, size_t b) { return items[a * 4 + 3] > items[b * 4 + 3]; });
+  out->clear();
+  for (size_t i : order) out->insert(out->end(), items.begin() + i * 4, items.begin() + i * 4 + 4);
+}
+
+int ensure_ablation() {
+  State& s = g_state;
+  if (s.abl) return FAS_OK;
+  const HostPlan& p = s.plan;
+  const int64_t npad = (p.N + 127) / 128 * 128;
+  std::vector<int32_t> w[2];
+  for (int pass = 0; pass < 2; ++pass) ablation_work(p, pass, &w[pass]);
+  const size_t o_bytes = (size_t)p.H * npad * p.d * 4, l_bytes = (size_t)p.H * npad * 4;
+  const size_t w_bytes[2] = {(w[0].size() * 4 + 255) / 256 * 256, (w[1].size() * 4 + 255) / 256 * 256};
+  if (cudaMalloc(&s.abl, 2 * o_bytes + 2 * l_bytes + w_bytes[0] + w_bytes[1] + 256) != cudaSuccess) {
+    s.abl = nullptr;
+    return FAS_ERR_CUDA;
+  }
+  uint8_t* b = static_cast<uint8_t*>(s.abl);
+  for (int pass = 0; pass < 2; ++pass) {
+    s.abl_o[pass] = reinterpret_cast<float*>(b);
+    b += o_bytes;
+  }
+  for (int pass = 0; pass < 2; ++pass) {
+    s.abl_lse[pass] = reinterpret_cast<float*>(b);
+    b += l_bytes;
+  }
+  for (int pass = 0; pass < 2; ++pass) {
+    s.abl_work[pass] = reinterpret_cast<int4*>(b);
+    s.abl_items[pass] = (int)(w[pass].size() / 4);
+    if (!w[pass].empty() &&
+        cudaMemcpy(s.abl_work[pass], w[pass].data(), w[pass].size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+      return FAS_ERR_CUDA;
+    b += w_bytes[pass];
+  }
+  s.abl_npad = npad;
+  return FAS_OK;
+}
+
+int check_device_plain() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FAS_ERR_CUDA;
+  return dev == g_state.device ? FAS_OK : FAS_ERR_STATE;
+}
+
+// The device error word the calls that need no plan report into: the
+// plan's when there is one, else one allocated on first use per device and
+// kept for the process.
+int error_word(unsigned int** out) {
+  if (g_state.planned && check_device_plain() == FAS_OK) {
+    *out = g_state.err;
+    return FAS_OK;
+  }
+  static unsigned int* words[64] = {nullptr};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FAS_ERR_CUDA;
+  if (!words[dev]) {
+    if (cudaMalloc(&words[dev], sizeof(unsigned int)) != cudaSuccess) return FAS_ERR_CUDA;
+    if (cudaMemset(words[dev], 0, sizeof(unsigned int)) != cudaSuccess) return FAS_ERR_CUDA;
+  }
+  *out = words[dev];
+  return FAS_OK;
+}
+
+int check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FAS_ERR_CUDA;
+  if (g_state.planned && dev != g_state.device) return FAS_ERR_STATE;
+  return FAS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fas_plan_describe(int frame_tokens, int n_frames, int ref_frames, int window_radius, int heads, int head_dim,
+                      int block_k, fas_plan_info* info, int32_t* table, int32_t* work) {
+  return describe(nullptr, frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k, info, table,
+                  work);
+}
+
+int fas_plan_describe_ragged(const int32_t* frame_tokens, int n_frames, int ref_frames, int window_radius,
+                             int heads, int head_dim, int block_k, fas_plan_info* info, int32_t* table,
+                             int32_t* work) {
+  if (!frame_tokens) return FAS_ERR_ARG;
+  return describe(frame_tokens, 0, n_frames, ref_frames, window_radius, heads, head_dim, block_k, info, table, work);
+}
+
+int fas_plan_ex(int frame_tokens, int n_frames, int ref_frames, int window_radius, int heads, int head_dim,
+                int block_k, fas_plan_info* info) {
+  return make_plan(nullptr, frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, block_k, info);
+}
+
 int fas_plan(int frame_tokens, int n_frames, int ref_frames, int window_radius, int heads, int head_dim,
              fas_plan_info* info) {
   return fas_plan_ex(frame_tokens, n_frames, ref_frames, window_radius, heads, head_dim, 0, info);
+}
+
+int fas_plan_ragged(const int32_t* frame_tokens, int n_frames, int ref_frames, int window_radius, int heads,
+                    int head_dim, int block_k, fas_plan_info* info) {
+  if (!frame_tokens) return FAS_ERR_ARG;
+  return make_plan(frame_tokens, 0, n_frames, ref_frames, window_radius, heads, head_dim, block_k, info);
 }
 
 int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_host) {
@@ -517,6 +672,127 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
   s.pre_k = s.dk;
   s.last_launches = launches;
   return FAS_OK;
+}
+
+int fas_forward_ablation(const void* q, const void* k, const void* v, void* out, float* lse, void* cuda_stream) {
+  if (!g_state.planned) return FAS_ERR_STATE;
+  if (!q || !k || !v || !out || !lse) return FAS_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return FAS_ERR_ALIGN;
+  const HostPlan& p = g_state.plan;
+  if (p.ragged || g_state.layout != FAS_LAYOUT_HND) return FAS_ERR_UNSUPPORTED;
+  int rc = check_device();
+  if (rc != FAS_OK) return rc;
+  rc = ensure_encoder();
+  if (rc != FAS_OK) return rc;
+  rc = ensure_ablation();
+  if (rc != FAS_OK) return rc;
+  State& s = g_state;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // Q, K and V as [H][N][d] with 128-row boxes: tiles of the padded sequence
+  // read zeros past N.
+  const cuuint64_t D = (cuuint64_t)p.d;
+  const cuuint64_t dims[3] = {D, (cuuint64_t)p.N, (cuuint64_t)p.H};
+  const cuuint64_t strides[2] = {D * 2, (cuuint64_t)p.N * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  CUtensorMap tq, tk, tv;
+  if (encode(&tq, q, 3, dims, strides, box) != FAS_OK || encode(&tk, k, 3, dims, strides, box) != FAS_OK ||
+      encode(&tv, v, 3, dims, strides, box) != FAS_OK)
+    return FAS_ERR_CUDA;
+  int launches = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    if (s.abl_items[pass] == 0) continue;  // no reference frames: no reference pass
+    fas::AblationParams a;
+    a.f.work = s.abl_work[pass];
+    a.f.table = nullptr;
+    a.f.spans = nullptr;
+    a.f.q_by_frame = 0;
+    a.f.row_bound = nullptr;
+    a.f.elig = nullptr;
+    a.f.out = nullptr;
+    a.f.out_row_stride = a.f.out_head_stride = 0;
+    a.f.lse = nullptr;
+    a.f.err = s.err;
+    a.f.N = p.N;
+    a.f.Bk = 128;
+    a.f.mode = FAS_MODE_ONLINE;
+    a.f.scale_log2 = (float)(1.4426950408889634 / sqrt((double)p.d));
+    a.f.limit_ns = fas::kWaitLimitNs;
+    a.o32 = s.abl_o[pass];
+    a.lse32 = s.abl_lse[pass];
+    a.Npad = s.abl_npad;
+    a.T = p.T;
+    a.R0 = p.R0;
+    a.r = p.r;
+    a.Nf = p.Nf;
+    a.pass = pass;
+    if (fas::launch_ablation_pass(p.d, tq, tk, tv, a, s.abl_items[pass], st) != cudaSuccess) return FAS_ERR_CUDA;
+    ++launches;
+  }
+  const bool two = s.abl_items[1] > 0;
+  if (fas::launch_ablation_merge(p.d, s.abl_o[0], s.abl_lse[0], two ? s.abl_o[1] : nullptr,
+                                 two ? s.abl_lse[1] : nullptr, static_cast<uint16_t*>(out), lse, p.H, p.N,
+                                 s.abl_npad, st) != cudaSuccess)
+    return FAS_ERR_CUDA;
+  s.last_launches = launches + 1;
+  return FAS_OK;
+}
+
+int fas_prologue(const void* x, const void* w_folded, const float* cos_tab, const float* sin_tab, int tokens,
+                 int width, int heads, int head_dim, float eps, void* q, void* k, void* v, int layout, int groups,
+                 int ranks, void* cuda_stream) {
+  if (!x || !w_folded || !cos_tab || !sin_tab || !q || !k || !v) return FAS_ERR_ARG;
+  if (tokens < 1 || width < 64 || width % 64 != 0 || (head_dim != 64 && head_dim != 128) || heads < 1 ||
+      fas::prologue_tile_cols(heads, head_dim) == 0 || !(eps >= 0.f))
+    return FAS_ERR_ARG;
+  if (layout != FAS_LAYOUT_HND && layout != FAS_LAYOUT_NHD && layout != FAS_LAYOUT_A2A) return FAS_ERR_ARG;
+  if (layout == FAS_LAYOUT_A2A && (groups < 1 || ranks < 1 || heads % (groups * ranks) != 0)) return FAS_ERR_ARG;
+  if ((int64_t)tokens * width > (int64_t)INT32_MAX * 64) return FAS_ERR_ARG;
+  for (const void* ptr : {x, w_folded, (const void*)cos_tab, (const void*)sin_tab, (const void*)q, (const void*)k,
+                          (const void*)v})
+    if (!aligned16(ptr)) return FAS_ERR_ALIGN;
+  int rc = ensure_encoder();
+  if (rc != FAS_OK) return rc;
+  unsigned int* err = nullptr;
+  rc = error_word(&err);
+  if (rc != FAS_OK) return rc;
+  // x: {C, N} with 64 x 128 boxes; W': {C, 3*H*d} with 64 x TN boxes (both
+  // K-major, 128-byte swizzle).  Rows of the last panel past N read zeros.
+  const int tn = fas::prologue_tile_cols(heads, head_dim);
+  const cuuint64_t xd[2] = {(cuuint64_t)width, (cuuint64_t)tokens};
+  const cuuint64_t xs[1] = {(cuuint64_t)width * 2};
+  const cuuint32_t xb[2] = {64, 128};
+  const cuuint64_t wd[2] = {(cuuint64_t)width, (cuuint64_t)3 * heads * head_dim};
+  const cuuint32_t wb[2] = {64, (cuuint32_t)tn};
+  CUtensorMap tx, tw;
+  if (encode(&tx, x, 2, xd, xs, xb) != FAS_OK || encode(&tw, w_folded, 2, wd, xs, wb) != FAS_OK) return FAS_ERR_CUDA;
+  fas::PrologueParams pp;
+  pp.q = q;
+  pp.k = k;
+  pp.v = v;
+  pp.cos_tab = cos_tab;
+  pp.sin_tab = sin_tab;
+  pp.tokens = tokens;
+  pp.width = width;
+  pp.heads = heads;
+  pp.head_dim = head_dim;
+  pp.layout = layout;
+  pp.groups = layout == FAS_LAYOUT_A2A ? groups : 1;
+  pp.ranks = layout == FAS_LAYOUT_A2A ? ranks : 1;
+  pp.eps = eps;
+  pp.err = err;
+  pp.limit_ns = fas::kWaitLimitNs;
+  const cudaError_t e = fas::launch_prologue(tx, tw, pp, static_cast<cudaStream_t>(cuda_stream));
+  g_state.last_launches = e == cudaSuccess ? 1 : 0;
+  return e == cudaSuccess ? FAS_OK : FAS_ERR_CUDA;
+}
+
+int fas_prologue_fold_weights(const void* w, const float* gamma, void* w_folded, int width, int out_features,
+                              void* cuda_stream) {
+  if (!w || !gamma || !w_folded || width < 1 || out_features < 1) return FAS_ERR_ARG;
+  const cudaError_t e = fas::launch_fold_weights(static_cast<const uint16_t*>(w), gamma,
+                                                 static_cast<uint16_t*>(w_folded), out_features, width,
+                                                 static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? FAS_OK : FAS_ERR_CUDA;
 }
 
 int fas_set_layout(int layout) {

@@ -104,6 +104,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // --------------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
                                             int c1, int c2) {
   asm volatile(
@@ -185,32 +193,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// Whole-warp variants: every lane runs the issuing code with identical
-// (warp-uniform) operands and one elected lane issues.  Keeping the issue
-// loop convergent and fully unrolled is what lets the tensor pipe run at
-// full rate; a divergent single-lane loop issues several times slower.
-__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // True in exactly one lane of the (fully active) warp.
 __device__ __forceinline__ bool elect_one() {
   uint32_t e;
@@ -220,14 +202,6 @@ __device__ __forceinline__ bool elect_one() {
       "selp.b32 %0, 1, 0, p;\n\t}"
       : "=r"(e));
   return e != 0;
-}
-
-__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-      : "memory");
 }
 
 // Copy a 128-row x 256-bit slice of a shared-memory matrix (described like
@@ -301,12 +275,6 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(saddr));
-  return r;
-}
-
 // Packed pair arithmetic (two fp32 lanes per instruction, sm_100 family).
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
   uint64_t r;
@@ -346,44 +314,9 @@ __device__ __forceinline__ void order_after(uint32_t (&r)[16], float after) {
                : "f"(after));
 }
 
-// 2^x for two lanes on the FMA and integer pipes instead of the
-// special-function unit.  Cody-Waite style range reduction: x = n + f with
-// n = rint(x) and f in [-1/2, 1/2]; 2^f is a cubic fitted to minimise the
-// largest relative error on that interval (iterated re-weighted least
-// squares, max relative error 7.5e-5, well under a bf16 half-ulp of 2^-9);
-// the result's exponent field is then raised by n with one integer add.
-// Adding 1.5 * 2^23 rounds x to an integer held in the low mantissa bits of
-// the sum, and those bits shifted left by 23 are exactly n << 23 (mod 2^32).
-// Inputs are clamped at -125 so that the result stays a normal number (the
-// exponent field cannot wrap); callers only pass x <= 16.
-__device__ __forceinline__ void ex2_poly_x2(float& y0, float& y1, float x0, float x1) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  constexpr float kC0 = 0.99992806f, kC1 = 0.69326097f, kC2 = 0.24261114f, kC3 = 0.055171672f;
-  x0 = fmaxf(x0, -125.0f);
-  x1 = fmaxf(x1, -125.0f);
-  uint32_t t0, t1, p0, p1;
-  asm("{\n\t.reg .b64 x, t, j, f, p, rr, nr, m1, c0, c1, c2, c3;\n\t"
-      "mov.b64 x, {%4, %5};\n\t"
-      "mov.b64 rr, {%6, %6};\n\t"
-      "mov.b64 nr, {%7, %7};\n\t"
-      "mov.b64 m1, {%8, %8};\n\t"
-      "mov.b64 c0, {%9, %9};\n\t"
-      "mov.b64 c1, {%10, %10};\n\t"
-      "mov.b64 c2, {%11, %11};\n\t"
-      "mov.b64 c3, {%12, %12};\n\t"
-      "add.rn.f32x2 t, x, rr;\n\t"
-      "add.rn.f32x2 j, t, nr;\n\t"
-      "fma.rn.f32x2 f, j, m1, x;\n\t"
-      "fma.rn.f32x2 p, f, c3, c2;\n\t"
-      "fma.rn.f32x2 p, p, f, c1;\n\t"
-      "fma.rn.f32x2 p, p, f, c0;\n\t"
-      "mov.b64 {%0, %1}, t;\n\t"
-      "mov.b64 {%2, %3}, p;\n\t}"
-      : "=r"(t0), "=r"(t1), "=r"(p0), "=r"(p1)
-      : "f"(x0), "f"(x1), "f"(kRound), "f"(-kRound), "f"(-1.0f), "f"(kC0), "f"(kC1), "f"(kC2), "f"(kC3));
-  y0 = __uint_as_float(p0 + (t0 << 23));
-  y1 = __uint_as_float(p1 + (t1 << 23));
-}
+// An empty instruction that reads a and b: what follows it is issued only
+// once both values (and the loads they came from) are complete.
+__device__ __forceinline__ void consume(float a, float b) { asm volatile("" ::"f"(a), "f"(b) : "memory"); }
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

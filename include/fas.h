@@ -69,7 +69,9 @@ enum {
 
 enum {
   FAS_LAYOUT_HND = 0, /* q, k, v, out contiguous [H, N, d] (head-major) */
-  FAS_LAYOUT_NHD = 1  /* q, k, v, out contiguous [N, H, d] (token-major) */
+  FAS_LAYOUT_NHD = 1, /* q, k, v, out contiguous [N, H, d] (token-major) */
+  FAS_LAYOUT_A2A = 2  /* fas_prologue only: a rank's token shard in the head-grouped all-to-all
+                         layout [G, P, n, H/(G*P), d] (see fas_prologue) */
 };
 
 enum {
@@ -112,6 +114,21 @@ int fas_plan(int frame_tokens, int n_frames, int ref_frames, int window_radius,
 int fas_plan_ex(int frame_tokens, int n_frames, int ref_frames, int window_radius,
                 int heads, int head_dim, int block_k, fas_plan_info* info);
 
+/* fas_plan_ex for frames of different spans (a ragged block table):
+ * frame_tokens points to R0 + F host int32 token counts, frame 0 first (the
+ * reference frames, then the video frames in time order); token j belongs
+ * to the frame whose token range [T_0 + .. + T_{g-1}, T_0 + .. + T_g) holds
+ * it.  Every count must be a positive multiple of 16.  The key block B_k is
+ * the largest multiple of 16 (at most 160) that divides every span, so no
+ * block straddles a frame boundary ("Deleting the Mask": blocks divide the
+ * frame's token span).  Visibility is the same frame rule as fas_plan.
+ * block_k = 0 chooses B_k; a nonzero block_k must divide every span.  The
+ * other calls take the ragged plan unchanged (q, k, v, out and lse have
+ * N = T_0 + .. + T_{Nf-1} tokens per head); fas_prepass_noalloc has no
+ * ragged form.  Query tiles of 128 rows stay inside one frame. */
+int fas_plan_ragged(const int32_t* frame_tokens, int n_frames, int ref_frames, int window_radius, int heads,
+                    int head_dim, int block_k, fas_plan_info* info);
+
 /* Host-only planning: the same plan fas_plan_ex would build, written to the
  * caller's buffers; touches no device and no library state.
  *   table (nullable): Nf * 4 int32 (see fas_plan_info.host_table);
@@ -121,9 +138,16 @@ int fas_plan_describe(int frame_tokens, int n_frames, int ref_frames, int window
                       int heads, int head_dim, int block_k, fas_plan_info* info,
                       int32_t* table, int32_t* work);
 
+/* fas_plan_describe for a ragged plan (frame_tokens as in fas_plan_ragged). */
+int fas_plan_describe_ragged(const int32_t* frame_tokens, int n_frames, int ref_frames, int window_radius,
+                             int heads, int head_dim, int block_k, fas_plan_info* info, int32_t* table,
+                             int32_t* work);
+
 /* Prepass ("Unchaining the Softmax": precomputed norms, mean-centred keys).
  * Reads q and k (device, bf16, in the current layout: [H, N, d] by
- * default) and computes per head the mean key mu_h, per key frame the
+ * default) once each from device memory (one kernel; the second pass over a
+ * head's keys is served from L2) and computes per head the mean key mu_h,
+ * per key frame the
  * largest centred key norm, and per row
  *   m_i = s q_i.mu_h + s |q_i| max_{visible frames g} max_{j in g} |k_j - mu_h|
  * (an upper bound on the row's largest scaled logit), plus the eligibility
@@ -131,7 +155,9 @@ int fas_plan_describe(int frame_tokens, int n_frames, int ref_frames, int window
  * bound and kbar_c(i) the mean centred key visible from row i; a head is
  * eligible when stat_h <= FAS_ELIG_SLACK_NATS.  Needs a plan.  elig_host
  * (nullable, H bytes, 1 = eligible): if set, the call synchronises the
- * stream, copies the bits and reports device timeouts. */
+ * stream, copies the bits and reports device timeouts.  A prepass whose
+ * bounded device wait gives up leaves every head ineligible (the online
+ * path, correct for any input) and sets the device error word. */
 int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_host);
 
 /* Attention.  q, k, v, out: device bf16 in the current layout ([H, N, d],
@@ -167,6 +193,26 @@ int fas_forward(const void* q, const void* k, const void* v, void* out, float* l
  * statistics. */
 int fas_forward_host(const void* q, const void* k, const void* v, void* out, float* lse,
                      int mode, int heads_per_group, void* cuda_stream);
+
+/* The splash-style ablation of fas_forward, for measuring what the
+ * frame-aligned single pass removes ("Deleting the Mask": the kernel the
+ * pages started from tiled the sequence in multiples of 128, so blocks
+ * straddle frame boundaries and need a mask predicate; padded the sequence
+ * to the tile grid; and ran the frame window and the reference frame as two
+ * attention passes writing full-precision intermediates that a merge pass
+ * re-read).  Same operation and results as fas_forward in FAS_MODE_ONLINE
+ * (within rounding): 128-row query tiles and 128-key blocks over the
+ * sequence padded to a multiple of 128, a per-element visibility test in
+ * every block a row does not see whole, online softmax, pass 1 over each
+ * tile's window keys and pass 2 over the reference keys, each writing
+ * O / sum(P) and the LSE in fp32 for every padded row (library-owned
+ * intermediates, 2 * H * Npad * (d + 1) * 4 bytes, allocated on first use
+ * per plan), then a merge kernel.  q, k, v, out: device bf16 [H, N, d];
+ * lse: device fp32 [H, N].  Needs a uniform plan (FAS_ERR_STATE without a
+ * plan) in the head-major layout; a ragged plan or the token-major layout
+ * returns FAS_ERR_UNSUPPORTED.  No prepass is needed.  Three launches
+ * (two when the plan has no reference frame), asynchronous on cuda_stream. */
+int fas_forward_ablation(const void* q, const void* k, const void* v, void* out, float* lse, void* cuda_stream);
 
 /* Memory layout of q, k, v and out for the calls that follow, on the
  * current plan: FAS_LAYOUT_HND ([H, N, d], the default of every new plan) or
@@ -212,8 +258,12 @@ int fas_selftest_wait_timeout(int limit_us, void* cuda_stream);
  * FAS_NOALLOC_SCRATCH_BYTES in device memory that the library image holds on
  * every GPU that loads it, until the process exits.
  *   q, k       : device bf16 [H, N, d] (head-major, whatever the current
- *                layout of the plan calls), 16-byte aligned;
- *   row_bound  : device fp32 [H, N], receives m_i (as fas_prepass_readback);
+ *                layout of the plan calls), 16-byte aligned, with exactly
+ *                N = (ref_frames + n_frames) * frame_tokens rows per head:
+ *                the call has no plan to check the buffers against, and
+ *                shorter buffers are read past their end;
+ *   row_bound  : device fp32 [H, N] (the same N), receives m_i (as
+ *                fas_prepass_readback);
  *   stat       : device fp32 [H], receives stat_h;
  *   elig       : device uint8 [H], receives the eligibility bits.
  * The geometry arguments follow fas_plan.  The scratch needed is about
@@ -221,15 +271,62 @@ int fas_selftest_wait_timeout(int limit_us, void* cuda_stream);
  * returns FAS_ERR_SCRATCH before any device work (e.g. 720p and 1080p SR
  * chunks with H = 24, d = 128 fit; H = 48 at 720p does not).
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
+ * (cudaGetSymbolAddress) with that device current, and again after the
+ * device's context has changed (a device reset); make that first call
  * before any stream capture.  All calls share the one array and leave their
- * values in it (every element is written before it is read, so nothing
- * needs clearing): calls that may overlap on the GPU — other streams, other
- * host threads — race and must be serialised by the caller.  Asynchronous
- * on cuda_stream; launch errors return FAS_ERR_CUDA. */
+ * values in it; each call clears, on cuda_stream, the counters, flags and
+ * error word it keeps there (and every other element is written before it
+ * is read): calls that may overlap on the GPU — other streams, other host
+ * threads — race and must be serialised by the caller.  Asynchronous on
+ * cuda_stream; launch errors return FAS_ERR_CUDA.  If a bounded device wait
+ * gives up, elig stays all zero (every head ineligible: the online path,
+ * correct for any input). */
 int fas_prepass_noalloc(const void* q, const void* k, int frame_tokens, int n_frames, int ref_frames,
                         int window_radius, int heads, int head_dim, float* row_bound, float* stat,
                         uint8_t* elig, void* cuda_stream);
+
+/* The attention prologue ("Layout Is the ABI", Fig. 5: normalization,
+ * rotary embeddings, projections and head packing fused into one kernel that
+ * writes exactly the layout the consumer reads).  For each token n:
+ *   y_n = (x_n / sqrt(mean(x_n^2) + eps) * gamma) W^T,   W: [3*H*d, C],
+ * output features [0, H*d) are q, [H*d, 2*H*d) k, the rest v, head h of each
+ * the d features from h*d; q and k are rotated per head, element i paired
+ * with i + d/2: (a, b) -> (a*cos - b*sin, a*sin + b*cos) with
+ * cos/sin[n, i]; v is as projected.  Rounded once to bf16 (nearest even).
+ * The projection runs on the tensor cores on the raw hidden states with
+ * the norm scale folded into the weight (fas_prologue_fold_weights) and
+ * 1/rms applied per row afterwards.
+ *   x         : device bf16 [tokens, width] (row-major), 16-byte aligned;
+ *   w_folded  : device bf16 [3*heads*head_dim, width] from
+ *               fas_prologue_fold_weights, 16-byte aligned;
+ *   cos_tab,
+ *   sin_tab   : device fp32 [tokens, head_dim/2], 16-byte aligned;
+ *   q, k, v   : device bf16 outputs, 16-byte aligned, in `layout`:
+ *               FAS_LAYOUT_HND [heads, tokens, d]; FAS_LAYOUT_NHD
+ *               [tokens, heads, d]; FAS_LAYOUT_A2A [groups, ranks, tokens,
+ *               heads/(groups*ranks), d], element [g, r, t, j] being token t
+ *               of head g*(heads/groups) + r*(heads/(groups*ranks)) + j (the
+ *               input of a head-grouped sequence-to-head all-to-all: group
+ *               g's slab [ranks, tokens, ...] is sent slice r to rank r);
+ *   groups,
+ *   ranks     : the A2A layout's G and P (ignored for the other layouts).
+ * Requirements: width a positive multiple of 64; head_dim in {64, 128};
+ * heads * head_dim a multiple of 128; for A2A heads divisible by
+ * groups * ranks; eps >= 0; tokens >= 1.  Otherwise FAS_ERR_ARG; pointer
+ * misalignment FAS_ERR_ALIGN.  Needs no plan.  One kernel, asynchronous on
+ * cuda_stream; a bounded device wait that gives up sets the error word of
+ * the current plan, if any (read by fas_status), and leaves the outputs
+ * incomplete. */
+int fas_prologue(const void* x, const void* w_folded, const float* cos_tab, const float* sin_tab, int tokens,
+                 int width, int heads, int head_dim, float eps, void* q, void* k, void* v, int layout, int groups,
+                 int ranks, void* cuda_stream);
+
+/* Folds the RMSNorm scale into the projection weight once, for
+ * fas_prologue: w_folded[o, c] = bf16(w[o, c] * gamma[c]) (nearest even).
+ * w, w_folded: device bf16 [out_features, width] (may not overlap);
+ * gamma: device fp32 [width].  Asynchronous on cuda_stream. */
+int fas_prologue_fold_weights(const void* w, const float* gamma, void* w_folded, int width, int out_features,
+                              void* cuda_stream);
 
 /* Kernel launches issued by the last fas_prepass / fas_forward call. */
 int fas_last_launch_count(void);

@@ -58,9 +58,9 @@ def sample_rows(w, per_head_min=512, seed=0):
 class Case:
     """Inputs on host and device, the plan, and oracle results (cached)."""
 
-    def __init__(self, w, rows=None):
+    def __init__(self, w, rows=None, x=None):
         self.w = w
-        self.x = workloads.generate(w)
+        self.x = workloads.generate(w) if x is None else x
         self.q, self.k, self.v = (to_dev(self.x[t]) for t in "qkv")
         self.rows = rows
         self._ref = None
@@ -139,6 +139,35 @@ def test_prepass_statistics(name):
     np.testing.assert_allclose(got["stat"], st["stat"], rtol=1e-4, atol=1e-3)
     assert np.array_equal(elig.astype(bool), st["elig"])
     assert np.array_equal(got["elig"].astype(bool), st["elig"])
+
+
+def test_prepass_statistics_720p():
+    """The fused prepass on the full 720p SR chunk (its queue interleaves
+    24 heads over three phases) against the oracle on every head."""
+    c = case("720p")
+    c.plan()
+    elig = fas.fas_prepass(c.q, c.k, want_elig=True)
+    got = fas.fas_prepass_readback(row_bound=True)
+    st = c.stats
+    np.testing.assert_allclose(got["mu"], st["mu"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["frame_max"], st["M"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["stat"], st["stat"], rtol=1e-4, atol=1e-3)
+    rows = c.rows
+    np.testing.assert_allclose(got["row_bound"][:, rows], st["m"][:, rows], rtol=1e-4, atol=2e-3)
+    assert np.array_equal(elig.astype(bool), st["elig"])
+
+
+def test_prepass_is_bit_reproducible():
+    """Whichever CTA finishes a phase reduces in a fixed order: two runs give
+    the same bits."""
+    c = case("mid")
+    c.plan()
+    outs = []
+    for _ in range(2):
+        fas.fas_prepass(c.q, c.k)
+        outs.append(fas.fas_prepass_readback(row_bound=True))
+    for key in outs[0]:
+        assert np.array_equal(outs[0][key], outs[1][key]), key
 
 
 @pytest.mark.parametrize("mode", ["auto", "online", "bounded"])
@@ -377,3 +406,123 @@ def test_forward_host_back_to_back_calls():
         assert fas.fas_status() == fas.FAS_OK
         assert torch.equal(o.view(torch.int16), od.cpu().view(torch.int16))
         assert torch.equal(l.view(torch.int32), ld.cpu().view(torch.int32))
+
+
+# Frames of different spans (a ragged block table): per-frame spans that
+# share a block size, query tiles clipped at each frame's own end.
+RAGGED = [
+    # name, H, d, R0, spans, r, sigma, seed
+    ("ragged_small", 2, 64, 1, [48, 32, 64, 16, 48, 80], 1, 2.0, 51),
+    ("ragged_mid", 3, 128, 1, [880, 720, 1040, 880, 560, 880, 1200], 2, 3.0, 52),
+    ("ragged_two_refs", 2, 128, 2, [208, 144, 272, 208, 336, 160], 1, 3.0, 53),
+    ("ragged_no_reference", 2, 128, 0, [288, 144, 432, 288, 96], 1, 3.0, 54),
+]
+
+
+def ragged_inputs(H, d, spans, sigma, seed):
+    """Seeded bf16 q, k, v for a ragged geometry: draw as for a uniform
+    workload with the same total token count."""
+    N = sum(spans)
+    w = workloads.Workload("ragged", H, d, 0, 1, N, 0, sigma, seed)  # one frame of N tokens: only the draws
+    return workloads.generate(w)
+
+
+@pytest.mark.parametrize("spec", RAGGED, ids=[e[0] for e in RAGGED])
+def test_ragged_frames_full_rows(spec):
+    name, H, d, R0, spans, r, sigma, seed = spec
+    F = len(spans) - R0
+    x = ragged_inputs(H, d, spans, sigma, seed)
+    q, k, v = (to_dev(x[t]) for t in "qkv")
+    info = fas.fas_plan(spans, F, R0, r, H, d)
+    assert info.visible_flops == ref.visible_flops(H, d, spans, F, R0, r)
+    want = ref.masked_attention(x["q"], x["k"], x["v"], spans, R0, r)
+    st = ref.bound_statistics(x["q"], x["k"], spans, R0, r)
+    elig = fas.fas_prepass(q, k, want_elig=True)
+    assert np.array_equal(elig.astype(bool), st["elig"])
+    got = fas.fas_prepass_readback(row_bound=True)
+    np.testing.assert_allclose(got["frame_max"], st["M"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["row_bound"], st["m"], rtol=1e-4, atol=1e-3)
+    for mode in ("auto", "online", "bounded"):
+        out, lse = fas.fas_forward(q, k, v, mode=mode)
+        assert fas.fas_status() == fas.FAS_OK
+        o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(l)), (name, mode)
+        assert np.abs(o - want["out"]).max() <= OUT_TOL, (name, mode)
+        assert np.abs(l - want["lse"]).max() <= LSE_TOL, (name, mode)
+    fas.fas_free()
+
+
+def test_ragged_frames_token_major_and_host_path():
+    """A ragged plan through the token-major layout and the host-buffer
+    entry point gives the head-major device path's bits."""
+    name, H, d, R0, spans, r, sigma, seed = RAGGED[1]
+    F = len(spans) - R0
+    x = ragged_inputs(H, d, spans, sigma, seed)
+    fas.fas_plan(spans, F, R0, r, H, d)
+    q, k, v = (to_dev(x[t]) for t in "qkv")
+    fas.fas_prepass(q, k)
+    out_h, lse_h = fas.fas_forward(q, k, v, mode="auto")
+    out_h, lse_h = out_h.cpu(), lse_h.cpu()
+    fas.fas_set_layout("nhd")
+    qn, kn, vn = (to_dev(to_nhd(x[t])) for t in "qkv")
+    fas.fas_prepass(qn, kn)
+    out_n, lse_n = fas.fas_forward(qn, kn, vn, mode="auto")
+    assert fas.fas_status() == fas.FAS_OK
+    assert torch.equal(out_n.cpu().transpose(0, 1).contiguous().view(torch.int16), out_h.view(torch.int16))
+    assert torch.equal(lse_n.cpu().view(torch.int32), lse_h.view(torch.int32))
+    fas.fas_set_layout("hnd")
+    o2, l2 = fas.fas_forward_host(*(host_bf16(x[t]) for t in "qkv"), mode="auto")
+    torch.cuda.current_stream().synchronize()
+    assert fas.fas_status() == fas.FAS_OK
+    assert torch.equal(o2.view(torch.int16), out_h.view(torch.int16))
+    assert torch.equal(l2.view(torch.int32), lse_h.view(torch.int32))
+    fas.fas_free()
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "720p"])
+def test_splash_ablation_matches_oracle(name):
+    """The splash-style ablation (128-multiple tiles over the padded
+    sequence, mask predicates, window and reference passes merged from fp32
+    intermediates) computes the same attention: within tolerance of the
+    oracle, and of the frame-aligned kernel's online path."""
+    c = case(name)
+    c.plan()
+    out, lse = fas.fas_forward_ablation(c.q, c.k, c.v)
+    assert fas.fas_status() == fas.FAS_OK
+    assert fas.fas_last_launch_count() == 3
+    c.check(out, lse, f"{name}/ablation")
+    # Every row (the oracle check samples the large workloads): each kernel
+    # is within the tolerance of the exact result, so the two are within
+    # twice it of each other.
+    _, out_o, lse_o = c.run("online")
+    assert (out.float() - out_o.float()).abs().max().item() <= 2 * OUT_TOL
+    assert (lse - lse_o).abs().max().item() <= 2 * LSE_TOL
+
+
+@pytest.mark.parametrize("spec", [e for e in EDGE if e[0] in ("no_reference", "two_references", "T16_r0",
+                                                             "d64_wide_window")], ids=lambda e: e[0])
+def test_splash_ablation_edge_geometries(spec):
+    name, H, d, R0, F, T, r, sigma, seed, bk = spec
+    c = Case(workloads.Workload(name, H, d, R0, F, T, r, sigma, seed))
+    c.plan()
+    out, lse = fas.fas_forward_ablation(c.q, c.k, c.v)
+    assert fas.fas_status() == fas.FAS_OK
+    assert fas.fas_last_launch_count() == (2 if R0 == 0 else 3)
+    c.check(out, lse, f"{name}/ablation")
+
+
+def test_splash_ablation_refuses_what_it_does_not_cover():
+    c = case("tiny")
+    c.plan()
+    lib = fas.load()
+    st = torch.cuda.current_stream().cuda_stream
+    out = torch.empty_like(c.q)
+    lse = torch.empty(c.w.heads, c.w.tokens, device="cuda")
+    fas.fas_set_layout("nhd")
+    assert lib.fas_forward_ablation(c.q.data_ptr(), c.k.data_ptr(), c.v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), st) == fas.FAS_ERR_UNSUPPORTED
+    fas.fas_set_layout("hnd")
+    fas.fas_plan([48, 32, 64], 2, 1, 1, 1, 64)
+    assert lib.fas_forward_ablation(c.q.data_ptr(), c.k.data_ptr(), c.v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), st) == fas.FAS_ERR_UNSUPPORTED
+    fas.fas_free()

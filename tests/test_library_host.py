@@ -41,9 +41,12 @@ def test_exports_every_declared_function(built_library):
 
 
 def test_library_is_built_for_sm_103a():
-    # The fatbin must carry sm_103a code; check the ELF note nvcc embeds.
-    data = open(fas.library_path(), "rb").read()
-    assert b"sm_103a" in data
+    """The build compiles every translation unit for sm_103a and nothing
+    else, and the built library is the one those flags produced."""
+    from frame_aligned_sparse_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    stamp = os.path.join(build.BUILD, "stamp")
+    assert open(stamp).read() == build._fingerprint()
 
 
 GEOMETRIES = [
@@ -99,6 +102,85 @@ def test_plan_covers_mask_exactly(geo):
         assert nblk == (table[f][1] + table[f][3]) // Bk
     assert np.all(np.diff(work[:, 3]) <= 0)
     assert info.key_blocks == int(work[:, 3].sum())
+
+
+RAGGED_GEOMETRIES = [
+    # (spans, R0, r, H, d)
+    ([48, 32, 64, 16, 48], 1, 1, 2, 64),
+    ([3600, 3520, 3600, 3680, 3600, 3440, 3600], 1, 2, 3, 128),
+    ([160, 320, 480, 160, 640], 2, 0, 1, 128),
+    ([96, 144, 48, 240, 192, 96], 0, 1, 2, 64),
+    ([880, 880, 704, 1056, 880], 1, 9, 1, 128),
+]
+
+
+@pytest.mark.parametrize("geo", RAGGED_GEOMETRIES, ids=lambda g: "Nf%d_R%d_r%d" % (len(g[0]), g[1], g[2]))
+def test_ragged_plan_covers_mask_exactly(geo):
+    """Frames of different spans: the block divides every span, no block
+    straddles a frame, every query frame's blocks cover exactly the oracle's
+    explicit mask, and the FLOP count is the oracle's."""
+    spans, R0, r, H, d = geo
+    F = len(spans) - R0
+    info, table, work = fas.fas_plan_describe(spans, F, R0, r, H, d)
+    Bk = info.block_k
+    assert all(t % Bk == 0 for t in spans) and Bk % 16 == 0 and Bk <= 160
+    assert all(any(t % b for t in spans) for b in range(Bk + 16, 161, 16)), "a larger block divides every span"
+    N = sum(spans)
+    starts = np.concatenate([[0], np.cumsum(spans)])
+    assert info.tokens == N and info.total_frames == len(spans)
+    for f in range(len(spans)):
+        covered = np.zeros(N, dtype=bool)
+        for b in expand_blocks(table[f], Bk):
+            g = np.searchsorted(starts, b, side="right") - 1
+            assert b + Bk <= starts[g + 1], "block straddles a frame boundary"
+            assert not covered[b:b + Bk].any(), "duplicate block"
+            covered[b:b + Bk] = True
+        rows = np.array([starts[f], starts[f + 1] - 1])
+        mask = ref.token_mask(rows, N, spans, R0, r)
+        assert np.array_equal(covered, mask[0]) and np.array_equal(covered, mask[1])
+    assert info.visible_flops == ref.visible_flops(H, d, spans, F, R0, r)
+    tiles = sum(-(-t // 128) for t in spans)
+    assert info.n_work == H * tiles == len(work)
+    assert len({(int(a), int(b), int(c)) for a, b, c, _ in work}) == info.n_work
+    for h, f, t, nblk in work:
+        assert t < -(-spans[f] // 128) and nblk == (table[f][1] + table[f][3]) // Bk
+    assert np.all(np.diff(work[:, 3]) <= 0)
+
+
+def test_ragged_plan_equal_spans_is_the_uniform_plan():
+    a = fas.fas_plan_describe(880, 16, 1, 2, 16, 128)
+    b = fas.fas_plan_describe([880] * 17, 16, 1, 2, 16, 128)
+    assert a[0].block_k == b[0].block_k and a[0].visible_flops == b[0].visible_flops
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("spans,R0,bk", [([48, 40, 64], 1, 0), ([48, 0, 64], 1, 0), ([48, 64], 2, 0),
+                                         ([48, 96, 64], 1, 32), ([48, 96, 64], 1, 48)])
+def test_bad_ragged_arguments_are_rejected(spans, R0, bk):
+    lib = fas.load()
+    info = fas._PlanInfoC()
+    arr = np.array(spans, dtype=np.int32)
+    F = len(spans) - R0
+    if F < 1:
+        F = 1  # the span count then does not match R0 + F
+        with pytest.raises(ValueError):
+            fas.fas_plan_describe(spans, F, R0, 1, 1, 64)
+        return
+    assert lib.fas_plan_describe_ragged(arr.ctypes.data, F, R0, 1, 1, 64, bk, ctypes.byref(info), None,
+                                        None) == fas.FAS_ERR_ARG
+
+
+def test_noalloc_wrapper_rejects_a_geometry_that_does_not_match_q():
+    """fas_prepass_noalloc has no plan to check its buffers against; the
+    binding refuses a geometry whose token count differs from q's before
+    anything reaches the device."""
+    import torch
+    q = torch.zeros(2, 9 * 48, 64, dtype=torch.bfloat16)
+    rb, stat, elig = torch.zeros(2, 9 * 48), torch.zeros(2), torch.zeros(2, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="rows per head"):
+        fas.fas_prepass_noalloc(q, q, 48, 9, 1, 1, rb, stat, elig)  # needs 10 * 48 rows
+    with pytest.raises(ValueError, match="rows per head"):
+        fas.fas_prepass_noalloc(q, q, 64, 8, 1, 1, rb, stat, elig)
 
 
 def test_block_size_choice_matches_frame_spans():

@@ -68,6 +68,39 @@ def test_noalloc_prepass_matches_allocating_prepass(lib, name):
         assert np.array_equal(results[0][key], results[1][key]), key
 
 
+# Geometries where the call's own frame rule (it has no block table) is most
+# likely to differ from the planner's: no reference frame, two reference
+# frames, a single video frame, a window wider than the clip.
+EDGE = [
+    # name, H, d, R0, F, T, r, sigma, seed
+    ("no_reference", 2, 128, 0, 5, 144, 1, 3.0, 32),
+    ("two_references", 1, 128, 2, 4, 208, 1, 3.0, 33),
+    ("single_frame", 1, 64, 1, 1, 256, 3, 2.0, 34),
+    ("d64_wide_window", 2, 64, 1, 9, 240, 9, 2.0, 38),
+]
+
+
+@pytest.mark.parametrize("spec", EDGE, ids=[e[0] for e in EDGE])
+def test_noalloc_prepass_edge_geometries(lib, spec):
+    name, H, d, R0, F, T, r, sigma, seed = spec
+    w = workloads.Workload(name, H, d, R0, F, T, r, sigma, seed)
+    x = workloads.generate(w, tensors=("q", "k"))
+    q, k = to_dev(x["q"]), to_dev(x["k"])
+    N = w.tokens
+    fas.fas_plan(T, F, R0, r, H, d)
+    fas.fas_prepass(q, k)
+    want = fas.fas_prepass_readback(row_bound=True)
+    for _ in range(2):
+        row_bound = torch.full((H, N), float("nan"), device="cuda")
+        stat = torch.full((H,), float("nan"), device="cuda")
+        elig = torch.full((H,), 255, dtype=torch.uint8, device="cuda")
+        fas.fas_prepass_noalloc(q, k, T, F, R0, r, row_bound, stat, elig)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(row_bound.cpu().numpy(), want["row_bound"], rtol=1e-4, atol=1e-3)
+        np.testing.assert_allclose(stat.cpu().numpy(), want["stat"], rtol=1e-4, atol=1e-3)
+        assert np.array_equal(elig.cpu().numpy(), want["elig"])
+
+
 def test_noalloc_rejects_problems_larger_than_its_scratch(lib):
     # 48 heads of the 720p geometry need about 5.5 MB of scratch (> 4 MiB).
     q = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
