@@ -152,8 +152,9 @@ def l2_note(qkv_bytes: int) -> str:
 
 
 KERNEL_SOURCES = {
-    "attention_fwd": ("attention.cu", "ptx.cuh", "kernels.h", "internal.h"),
+    "attention_fwd": ("attention.cu", "attention_core.cuh", "ptx.cuh", "kernels.h", "internal.h"),
     "prepass_kernel": ("prepass.cu", "kernels.h", "internal.h"),
+    "prologue_qkv": ("prologue.cu", "ptx.cuh", "kernels.h", "internal.h"),
 }
 
 

@@ -69,7 +69,6 @@ struct State {
 };
 
 State g_state;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // Heads per group of fas_forward_host's default schedule in steady state:
 // large enough that each group's attention launch fills the GPU many times
 // over.  The schedule ramps up to it (1, 2, 4, ... heads) so that the first
@@ -182,26 +181,10 @@ int allocate(const HostPlan& p) {
   return FAS_OK;
 }
 
-int ensure_encoder() {
-  if (g_encode) return FAS_OK;
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-          cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || fn == nullptr)
-    return FAS_ERR_CUDA;
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  return FAS_OK;
-}
-
 // bf16 tensor map with 128-byte swizzle; dims innermost first.
 int encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
            const cuuint32_t* box) {
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes,
-                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FAS_OK : FAS_ERR_CUDA;
+  return fas::bf16_tensor_map(map, base, rank, dims, strides_bytes, box);
 }
 
 // Element strides of q, k, v and out in the current layout: between two
@@ -587,8 +570,6 @@ int fas_forward(const void* q, const void* k, const void* v, void* out, float* l
   if (mode != FAS_MODE_ONLINE && (q != g_state.pre_q || k != g_state.pre_k)) return FAS_ERR_STATE;
   int rc = check_device();
   if (rc != FAS_OK) return rc;
-  rc = ensure_encoder();
-  if (rc != FAS_OK) return rc;
   const HostPlan& p = g_state.plan;
   State& s = g_state;
   CUtensorMap tq, tk, tv;
@@ -607,8 +588,6 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
   if (heads_per_group < 0 || heads_per_group > p.H) return FAS_ERR_ARG;
   const int hg = heads_per_group;
   int rc = check_device();
-  if (rc != FAS_OK) return rc;
-  rc = ensure_encoder();
   if (rc != FAS_OK) return rc;
   rc = ensure_host_pipeline(hg);
   if (rc != FAS_OK) return rc;
@@ -682,8 +661,6 @@ int fas_forward_ablation(const void* q, const void* k, const void* v, void* out,
   if (p.ragged || g_state.layout != FAS_LAYOUT_HND) return FAS_ERR_UNSUPPORTED;
   int rc = check_device();
   if (rc != FAS_OK) return rc;
-  rc = ensure_encoder();
-  if (rc != FAS_OK) return rc;
   rc = ensure_ablation();
   if (rc != FAS_OK) return rc;
   State& s = g_state;
@@ -750,10 +727,8 @@ int fas_prologue(const void* x, const void* w_folded, const float* cos_tab, cons
   for (const void* ptr : {x, w_folded, (const void*)cos_tab, (const void*)sin_tab, (const void*)q, (const void*)k,
                           (const void*)v})
     if (!aligned16(ptr)) return FAS_ERR_ALIGN;
-  int rc = ensure_encoder();
-  if (rc != FAS_OK) return rc;
   unsigned int* err = nullptr;
-  rc = error_word(&err);
+  const int rc = error_word(&err);
   if (rc != FAS_OK) return rc;
   // x: {C, N} with 64 x 128 boxes; W': {C, 3*H*d} with 64 x TN boxes (both
   // K-major, 128-byte swizzle).  Rows of the last panel past N read zeros.
@@ -762,7 +737,7 @@ int fas_prologue(const void* x, const void* w_folded, const float* cos_tab, cons
   const cuuint64_t xs[1] = {(cuuint64_t)width * 2};
   const cuuint32_t xb[2] = {64, 128};
   const cuuint64_t wd[2] = {(cuuint64_t)width, (cuuint64_t)3 * heads * head_dim};
-  const cuuint32_t wb[2] = {64, (cuuint32_t)tn};
+  const cuuint32_t wb[2] = {64, (cuuint32_t)(tn / fas::prologue_cluster())};  // each CTA loads its share
   CUtensorMap tx, tw;
   if (encode(&tx, x, 2, xd, xs, xb) != FAS_OK || encode(&tw, w_folded, 2, wd, xs, wb) != FAS_OK) return FAS_ERR_CUDA;
   fas::PrologueParams pp;

@@ -8,8 +8,11 @@ namespace fas {
 
 constexpr int kQTile = 128;        // query rows per work item (MMA M)
 constexpr int kMaxBlockK = 160;    // largest key block: TMEM (O, two S buffers, Q) and the softmax registers
-constexpr int kPrepassRows = 512;       // rows per prepass work item, at most (items never cross frames)
-constexpr int kPrepassCtasPerSm = 4;    // resident prepass CTAs per SM
+#ifndef FAS_PREPASS_ROWS
+#define FAS_PREPASS_ROWS 1024
+#endif
+constexpr int kPrepassRows = FAS_PREPASS_ROWS;  // rows per prepass work item, at most (items never cross frames)
+constexpr int kPrepassCtasPerSm = 4;            // resident prepass CTAs per SM
 
 struct HostPlan {
   int T = 0, F = 0, R0 = 0, r = 0, H = 0, d = 0;  // T: the frame span (the largest one when ragged)

@@ -18,6 +18,11 @@ constexpr unsigned int kErrWaitPrepass = 32u;
 // Bound on any single device-side wait in the attention kernel.
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
 
+// A bf16 tensor map with 128-byte swizzle (dims innermost first); returns a
+// FAS_* status.
+int bf16_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                    const cuuint64_t* strides_bytes, const cuuint32_t* box);
+
 struct PrepassArgs {
   const void* q;        // bf16, row (h, j) at q + h * head_stride + j * row_stride
   const void* k;        // bf16, same layout as q
@@ -118,6 +123,9 @@ struct PrologueParams {
 // Output features per tile of the prologue kernel for H heads of d (0 when
 // H * d is not a multiple of 128).
 int prologue_tile_cols(int heads, int head_dim);
+
+// CTAs per cluster of the prologue kernel (they share each weight tile).
+int prologue_cluster();
 
 cudaError_t launch_prologue(const CUtensorMap& tx, const CUtensorMap& tw, const PrologueParams& p,
                             cudaStream_t stream);

@@ -14,17 +14,23 @@
 // Since the mean of the visible centred logits is at most their maximum,
 // G_i bounds the gap between b_i and the true centred row maximum.
 //
-// One persistent kernel.  Work items are (phase, head, frame, chunk of rows
-// of that frame), taken from a queue in the order
+// One persistent kernel, four 256-thread CTAs per SM.  Work items are
+// (phase, head, frame, chunk of at most 1024 rows of that frame), taken from
+// a queue in the order
 //     keys(h)  centred(h-L)  queries(h-2L)    for h = 0, 1, ..., H+2L-1
-// with a lag of L = 2 heads between phases: by the time a head's centred
-// (or query) items come out of the queue its keys (or centred) items have
-// finished, so items rarely wait, while the two heads' keys between their
-// first and second read (about 40 MB at the 720p geometry) stay in L2.
 //   keys:     column sums of the chunk's keys;
-//   centred:  max |k_j - mu_h| over the chunk (needs mu_h);
+//   centred:  max |k_j - mu_h|^2 over the chunk (needs mu_h);
 //   queries:  m_i and the max of G_i over the chunk (needs the window
 //             statistics of head h).
+// With a lag of L = 2 heads between phases, by the time a head's centred
+// (or query) items come out of the queue its keys (or centred) items have
+// finished, so items rarely wait, while the two heads' keys between their
+// first and second read (about 40 MB at the 720p geometry) stay in L2: K is
+// read from DRAM once, and the prepass moves one K and one Q from HBM plus
+// the small outputs.  An item's fixed costs (taking it from the queue,
+// waiting for its head's flag, the reductions and completion counts) are a
+// chain of dependent steps; four CTAs per SM run four such chains at once,
+// and large items spread each chain's cost over more bytes.
 // Completion is counted per frame and per head: the item that completes a
 // frame reduces its chunks' results, and the item that completes the last
 // frame of a head reduces the frames and publishes the next phase's inputs:
@@ -33,9 +39,6 @@
 // eligibility bit after the queries.  These reductions sit on the critical
 // path of every head, so they keep many loads in flight and add in a fixed
 // order.  A consumer item polls the head's ready flag with a bounded wait.
-// The queue order keeps each head's keys in L2 between their two reads (one
-// head is about 20 MB at the 720p geometry), so K is read from DRAM once:
-// the prepass moves one K and one Q from HBM, plus the small outputs.
 //
 // All loads are 16-byte vectors, one row shared by d/8 consecutive lanes
 // (each row's d values are contiguous), consecutive rows over the block.

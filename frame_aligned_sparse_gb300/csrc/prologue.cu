@@ -21,6 +21,8 @@
 // output features in tiles of TN = 256 (or 128) on the tensor cores:
 //   warp 0     TMA producer: x tile [128 x 64] and W' tile [TN x 64] per
 //              K-step of 64 (128B-swizzled, K-major) into a 4-stage ring;
+//              the CTAs of a cluster (consecutive panels of one part) load
+//              a share of each W' tile and multicast it to all of them;
 //   warp 1     TMEM allocator and MMA issuer (one elected lane):
 //              tcgen05.mma kind::f16, M = 128, N = TN, both operands from
 //              shared memory, fp32 accumulators in TMEM, two accumulator
@@ -44,6 +46,10 @@
 namespace fas {
 namespace {
 
+#ifndef FAS_PROLOGUE_CLUSTER
+#define FAS_PROLOGUE_CLUSTER 2
+#endif
+constexpr int kClusterP = FAS_PROLOGUE_CLUSTER;  // CTAs that share each W' tile (TMA multicast)
 constexpr int kThreadsP = 192;
 constexpr int kStagesP = 4;
 constexpr int kKStep = 64;   // K elements per stage: one 128-byte swizzle row of bf16
@@ -58,7 +64,6 @@ struct PBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int skip;
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -76,7 +81,7 @@ __device__ __forceinline__ int64_t out_offset(const PrologueParams& p, int h, in
   return ((int64_t)h * p.tokens + n) * D;  // FAS_LAYOUT_HND
 }
 
-template <int D, int TN>
+template <int D, int TN, int CL>
 __global__ void __launch_bounds__(kThreadsP, 1)
     prologue_qkv(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                  const PrologueParams p) {
@@ -91,12 +96,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   const uint32_t ring = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
   uint8_t* const ring_ptr = smem_raw + (ring - ptx::smem_addr(smem_raw));
 
-  if (threadIdx.x == 0) bars.skip = *reinterpret_cast<volatile unsigned int*>(p.err) != 0u;
-  __syncthreads();
-  if (bars.skip) return;
-
+  // The CTAs of a cluster take consecutive panels of the same part, so they
+  // need the same W' tiles: each loads 1/CL of every W' tile and multicasts
+  // it to all of them, and each one's MMAs free a stage in all of them.
+  // (No early exit here: a CTA of a cluster must take part in the whole
+  // exchange; the error word is looked at by the bounded waits.)
+  const uint32_t rank = CL > 1 ? ptx::cluster_ctarank() : 0u;
+  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int panel = blockIdx.x / 3, part = blockIdx.x % 3;
+  const int cid = blockIdx.x / CL;
+  const int part = cid % 3, panel = (cid / 3) * CL + (int)rank;
   const int ksteps = p.width / kKStep;
   const int ncol = p.heads * D / TN;
   volatile int* abort_flag = &bars.abort;
@@ -104,7 +113,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesP; ++s) {
       ptx::mbar_init(ptx::smem_addr(&bars.full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&bars.empty[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&bars.empty[s]), CL);  // the MMAs of every CTA of the cluster
       ptx::mbar_init(ptx::smem_addr(&bars.rowsum[s]), kRows);
     }
     for (int b = 0; b < 2; ++b) {
@@ -123,12 +132,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   ptx::tc_fence_before_sync();
   __syncthreads();
   ptx::tc_fence_after_sync();
+  if (CL > 1) ptx::cluster_sync();  // every CTA's barriers exist before any multicast reaches them
   const uint32_t tmem = bars.tmem_base;
 
   if (warp == 0) {
     if (lane == 0) {
       // Producer: fill f goes to stage f % S after the stage's previous fill
-      // is consumed by the MMAs (and, for first-tile fills, by the row sums).
+      // is consumed by the MMAs of every CTA of the cluster (and, for
+      // first-tile fills, by this CTA's row sums).
       int fill = 0;
       bool ok = true;
       for (int n = 0; ok && n < ncol; ++n)
@@ -147,7 +158,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           const uint32_t fb = ptx::smem_addr(&bars.full[s]);
           ptx::mbar_arrive_expect_tx(fb, kStageBytes);
           ptx::tma_load_2d(dst, &tm_x, fb, kk * kKStep, panel * kRows);
-          ptx::tma_load_2d(dst + kABytes, &tm_w, fb, kk * kKStep, part * p.heads * D + n * TN);
+          if (CL == 1)
+            ptx::tma_load_2d(dst + kABytes, &tm_w, fb, kk * kKStep, part * p.heads * D + n * TN);
+          else
+            ptx::tma_load_2d_multicast(dst + kABytes + rank * (kBBytes / CL), &tm_w, fb, kk * kKStep,
+                                       part * p.heads * D + n * TN + (int)rank * (TN / CL), kMask);
         }
       if (!ok) {
         // Let the copies already started land before the CTA exits (a
@@ -186,7 +201,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           for (int k = 0; k < kKStep / 16; ++k)
             ptx::mma_ss(tmem + b * kAccCols, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), kIdesc,
                         (kk > 0 || k > 0) ? 1u : 0u);
-          ptx::mma_commit(ptx::smem_addr(&bars.empty[s]));
+          if (CL == 1)
+            ptx::mma_commit(ptx::smem_addr(&bars.empty[s]));
+          else
+            ptx::mma_commit_multicast(ptx::smem_addr(&bars.empty[s]), kMask);
         }
         if (ok) ptx::mma_commit(ptx::smem_addr(&bars.acc_full[b]));
       }
@@ -305,6 +323,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     ptx::tc_fence_after_sync();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
+  // A CTA's shared memory must outlive the other CTAs' multicasts and
+  // commits into it.
+  if (CL > 1) ptx::cluster_sync();
 }
 
 // W'[o, c] = bf16(W[o, c] * gamma[c]), rounded to nearest even.
@@ -321,14 +342,31 @@ __global__ void fold_weights(const uint16_t* __restrict__ w, const float* __rest
 template <int D, int TN>
 cudaError_t launch_pd(const CUtensorMap& tx, const CUtensorMap& tw, const PrologueParams& p, cudaStream_t st) {
   const size_t smem = 1024 + (size_t)kStagesP * (kRows + TN) * kKStep * 2;
-  cudaError_t e = cudaFuncSetAttribute(prologue_qkv<D, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = prologue_qkv<D, TN, kClusterP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t panels = (p.tokens + kRows - 1) / kRows;
-  prologue_qkv<D, TN><<<(unsigned)(panels * 3), kThreadsP, smem, st>>>(tx, tw, p);
+  const int64_t clusters = (panels + kClusterP - 1) / kClusterP * 3;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(clusters * kClusterP));
+  cfg.blockDim = dim3(kThreadsP);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterP;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tx, tw, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int prologue_cluster() { return kClusterP; }
 
 int prologue_tile_cols(int heads, int head_dim) {
   const int f = heads * head_dim;
