@@ -12,7 +12,10 @@ constexpr int kMaxBlockK = 160;    // largest key block: TMEM (O, two S buffers,
 #define FAS_PREPASS_ROWS 1024
 #endif
 constexpr int kPrepassRows = FAS_PREPASS_ROWS;  // rows per prepass work item, at most (items never cross frames)
-constexpr int kPrepassCtasPerSm = 4;            // resident prepass CTAs per SM
+#ifndef FAS_PREPASS_CTAS
+#define FAS_PREPASS_CTAS 4
+#endif
+constexpr int kPrepassCtasPerSm = FAS_PREPASS_CTAS;  // resident prepass CTAs per SM (bounds its registers)
 
 struct HostPlan {
   int T = 0, F = 0, R0 = 0, r = 0, H = 0, d = 0;  // T: the frame span (the largest one when ragged)

@@ -22,10 +22,12 @@
 //   centred:  max |k_j - mu_h|^2 over the chunk (needs mu_h);
 //   queries:  m_i and the max of G_i over the chunk (needs the window
 //             statistics of head h).
-// With a lag of L = 2 heads between phases, by the time a head's centred
+// With a lag of L = 3 heads between phases, by the time a head's centred
 // (or query) items come out of the queue its keys (or centred) items have
-// finished, so items rarely wait, while the two heads' keys between their
-// first and second read (about 40 MB at the 720p geometry) stay in L2: K is
+// finished, so items rarely wait.  Keys are first read with an evict-last
+// L2 policy and read the second time (like the queries) with evict-first,
+// so that the L heads' keys between their two reads (about 60 MB at the
+// 720p geometry) stay in L2 while the query stream passes through: K is
 // read from DRAM once, and the prepass moves one K and one Q from HBM plus
 // the small outputs.  An item's fixed costs (taking it from the queue,
 // waiting for its head's flag, the reductions and completion counts) are a
@@ -64,7 +66,7 @@ constexpr int kUnroll = 4;  // 16-byte loads in flight per thread in a sweep
 enum Phase { kKeys = 0, kCentred = 1, kQueries = 2 };
 
 #ifndef FAS_PREPASS_LAG
-#define FAS_PREPASS_LAG 2
+#define FAS_PREPASS_LAG 3
 #endif
 constexpr int kLag = FAS_PREPASS_LAG;  // heads between consecutive phases in the queue
 
@@ -77,17 +79,9 @@ __device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8]) {
   }
 }
 
-// 16-byte load through L2, not kept in L1 (each row is read once per phase).
-__device__ __forceinline__ uint4 ld_keep(const uint4* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-// The same, marking the line as the first to evict from L2 (its last use).
-__device__ __forceinline__ uint4 ld_last(const uint4* p, uint64_t policy) {
+// 16-byte load through L2 with an L2 eviction policy, not kept in L1 (each
+// row is read once per phase).
+__device__ __forceinline__ uint4 ld_policy(const uint4* p, uint64_t policy) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
@@ -95,6 +89,15 @@ __device__ __forceinline__ uint4 ld_last(const uint4* p, uint64_t policy) {
   return r;
 }
 
+// Keys' first read: keep the line in L2 ahead of other lines (its second
+// read comes L heads later).
+__device__ __forceinline__ uint64_t evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// A line's last use (keys' second read, queries): first to leave L2.
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -218,7 +221,7 @@ __device__ __forceinline__ void publish(unsigned* flag) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) prepass_kernel(const PrepassArgs a) {
+__global__ void __launch_bounds__(kThreads, kPrepassCtasPerSm) prepass_kernel(const PrepassArgs a) {
   constexpr int VPR = D / 8;              // 16-byte vectors per row
   constexpr int RPI = kThreads / VPR;     // rows per sweep
   __shared__ Shared sh;
@@ -238,6 +241,7 @@ __global__ void __launch_bounds__(kThreads) prepass_kernel(const PrepassArgs a) 
   const uint4* const k = static_cast<const uint4*>(a.k);
   const int64_t rstride = a.row_stride / 8, hstride = a.head_stride / 8;  // in 16-byte vectors
   const uint64_t last_use = evict_first_policy();
+  const uint64_t reused = evict_last_policy();
 
   for (;;) {
     if (threadIdx.x == 0) {
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(kThreads) prepass_kernel(const PrepassArgs a) 
       for (; r + 3 * RPI < rows; r += 4 * RPI) {
         uint4 x[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) x[u] = ld_keep(base + (int64_t)(r + u * RPI) * rstride);
+        for (int u = 0; u < 4; ++u) x[u] = ld_policy(base + (int64_t)(r + u * RPI) * rstride, reused);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float f[8];
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) prepass_kernel(const PrepassArgs a) 
       }
       for (; r < rows; r += RPI) {
         float f[8];
-        unpack8(ld_keep(base + (int64_t)r * rstride), f);
+        unpack8(ld_policy(base + (int64_t)r * rstride, reused), f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] += f[e];
       }
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(kThreads) prepass_kernel(const PrepassArgs a) 
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int r = r0 + u * RPI + rs;
-          x[u] = r < rows ? ld_last(base + (int64_t)r * rstride, last_use) : make_uint4(0, 0, 0, 0);
+          x[u] = r < rows ? ld_policy(base + (int64_t)r * rstride, last_use) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(kThreads) prepass_kernel(const PrepassArgs a) 
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int r = r0 + u * RPI + rs;
-          x[u] = r < rows ? ld_last(base + (int64_t)r * rstride, last_use) : make_uint4(0, 0, 0, 0);
+          x[u] = r < rows ? ld_policy(base + (int64_t)r * rstride, last_use) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {

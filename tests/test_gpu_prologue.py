@@ -169,3 +169,44 @@ def test_prologue_argument_errors():
     assert lib.fas_prologue(*args, 128, 128, 2, 64, 1e-6, *o3, 7, 1, 1, st) == fas.FAS_ERR_ARG  # layout
     assert lib.fas_prologue(x.data_ptr() + 2, *args[1:], 128, 128, 2, 64, 1e-6, *o3, 0, 1, 1,
                             st) == fas.FAS_ERR_ALIGN
+
+
+def test_ulysses_one_rank_with_the_library_kernels():
+    """The head-grouped Ulysses schedule with the library's kernels as the
+    attention, on a one-rank NCCL group (each box has one GPU): the prologue
+    writes q, k, v in the all-to-all layout, every group's slab goes through
+    NCCL's all-to-all, and the per-group attention (token-major, hp heads)
+    gives bit for bit what one call over all heads gives."""
+    import os
+    import socket
+    import torch.distributed as dist
+    from frame_aligned_sparse_gb300 import ulysses
+
+    c = Inputs("mid")
+    w = c.w
+    G = 4
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        _, (qa, ka, va) = c.run("a2a", groups=G, ranks=1)
+        fn = ulysses.fas_attention_fn(w.frame_tokens, w.n_frames, w.ref_frames, w.window_radius, w.heads // G,
+                                      w.head_dim)
+        out, lse = ulysses.ulysses_attention(qa, ka, va, fn)
+        torch.cuda.synchronize()
+        assert fas.fas_status() == fas.FAS_OK
+        got = ulysses.from_a2a_layout(out)  # [N, H, d]
+        _, (q, k, v) = c.run("nhd")
+        fas.fas_plan(w.frame_tokens, w.n_frames, w.ref_frames, w.window_radius, w.heads, w.head_dim)
+        fas.fas_set_layout("nhd")
+        fas.fas_prepass(q, k)
+        want, want_lse = fas.fas_forward(q, k, v, mode="auto")
+        assert fas.fas_status() == fas.FAS_OK
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+        assert torch.equal(lse.reshape(w.heads, -1).view(torch.int32), want_lse.view(torch.int32))
+    finally:
+        fas.fas_set_layout("hnd")
+        fas.fas_free()
+        dist.destroy_process_group()
