@@ -67,6 +67,24 @@ def max_over_ranks(ms: float, device=None) -> float:
     return float(t.item())
 
 
+def pinned_copy_gbs(host_in, host_out, dev_buf, stream):
+    """GB/s of one pinned host->device copy of host_in and one device->host
+    copy into host_out (each the larger of two timings), on the stream."""
+    res = []
+    for src, dst in ((host_in, dev_buf), (dev_buf, host_out)):
+        best = 0.0
+        for _ in range(2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                dst.copy_(src, non_blocking=True)
+                b.record(stream)
+            b.synchronize()
+            best = max(best, src.numel() * src.element_size() / (a.elapsed_time(b) * 1e6))
+        res.append(best)
+    return res
+
+
 def job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
     """Whole-job throughput: every rank runs its own chunk (replicas, weak
     scaling), so the job does world * steps chunks in the slowest rank's
@@ -393,6 +411,7 @@ def run_fas(args, w):
     e2e_ms = max_over_ranks(e2e_ms, dev)
     h2d = sum(pin[t].numel() * 2 for t in "qkv")
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    copy_gbs = pinned_copy_gbs(pin["q"], out_h, q, stream)
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
@@ -491,7 +510,12 @@ def run_fas(args, w):
                      "traffic": recorded_traffic("attention_fwd", w.name)},
         "cpu_baseline": cpu,
         "e2e": {"value": job_tflops(world, flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / e2e_steps,
+                # Copy bandwidth between these pinned buffers and the device,
+                # taken outside the timed region: the host side of the box
+                # sets how far the copies can hide behind the kernels.
+                "pinned_h2d_gbs": copy_gbs[0], "pinned_d2h_gbs": copy_gbs[1]},
         "gpu_launches": timed_launches,
         "clocks": clocks,
         "ablation": abl,

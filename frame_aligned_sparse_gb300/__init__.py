@@ -30,6 +30,7 @@ __all__ = [
 
 FAS_OK, FAS_ERR_ARG, FAS_ERR_STATE, FAS_ERR_ALIGN, FAS_ERR_CUDA, FAS_ERR_TIMEOUT, FAS_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 FAS_ERR_SCRATCH = -7
+FAS_ERR_BOUND = -8
 FAS_NOALLOC_SCRATCH_BYTES = 4 << 20
 MODES = {"auto": 0, "online": 1, "bounded": 2}
 LAYOUTS = {"hnd": 0, "nhd": 1}  # q, k, v, out as [H, N, d] or [N, H, d]
@@ -372,9 +373,11 @@ def fas_free() -> None:
 
 
 def fas_status(stream=None) -> int:
-    """Synchronises the stream; returns FAS_OK or FAS_ERR_TIMEOUT (raises on other errors)."""
+    """Synchronises the stream; returns FAS_OK, FAS_ERR_TIMEOUT (a device wait
+    gave up) or FAS_ERR_BOUND (a bounded row's softmax sum left its safe
+    range: q or k changed since the prepass); raises on other errors."""
     rc = load().fas_status(_stream_handle(stream))
-    if rc not in (FAS_OK, FAS_ERR_TIMEOUT):
+    if rc not in (FAS_OK, FAS_ERR_TIMEOUT, FAS_ERR_BOUND):
         _check("fas_status", rc)
     return rc
 

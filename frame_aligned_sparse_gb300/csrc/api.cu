@@ -41,6 +41,7 @@ struct State {
   uint8_t* elig = nullptr;
   unsigned int* sync = nullptr;
   unsigned int* err = nullptr;
+  unsigned int* flags = nullptr;  // kFlagBoundRange (attention); cleared by fas_status
   const void* pre_q = nullptr;
   const void* pre_k = nullptr;
   int last_launches = 0;
@@ -158,6 +159,7 @@ int allocate(const HostPlan& p) {
       {H, (void**)&s.elig},
       {fas::prepass_sync_words(p.H, p.Nf) * 4, (void**)&s.sync},
       {sizeof(unsigned int), (void**)&s.err},
+      {sizeof(unsigned int), (void**)&s.flags},
   };
   size_t total = 0;
   for (auto& pt : parts) total += (pt.bytes + 255) & ~(size_t)255;
@@ -279,6 +281,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   fp.out_head_stride = head_stride();
   fp.lse = lse;
   fp.err = s.err;
+  fp.flags = s.flags;
   fp.N = p.N;
   fp.Bk = p.Bk;
   fp.mode = mode;
@@ -689,6 +692,7 @@ int fas_forward_ablation(const void* q, const void* k, const void* v, void* out,
     a.f.out_row_stride = a.f.out_head_stride = 0;
     a.f.lse = nullptr;
     a.f.err = s.err;
+    a.f.flags = s.flags;
     a.f.N = p.N;
     a.f.Bk = 128;
     a.f.mode = FAS_MODE_ONLINE;
@@ -793,11 +797,13 @@ int fas_free(void) {
 int fas_status(void* cuda_stream) {
   if (!g_state.planned) return FAS_ERR_STATE;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return FAS_ERR_CUDA;
-  unsigned int e = 0;
+  unsigned int e = 0, f = 0;
   if (cudaMemcpy(&e, g_state.err, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess) return FAS_ERR_CUDA;
-  if (e == 0) return FAS_OK;
-  if (cudaMemset(g_state.err, 0, sizeof(e)) != cudaSuccess) return FAS_ERR_CUDA;
-  return FAS_ERR_TIMEOUT;
+  if (cudaMemcpy(&f, g_state.flags, sizeof(f), cudaMemcpyDeviceToHost) != cudaSuccess) return FAS_ERR_CUDA;
+  if (e == 0 && f == 0) return FAS_OK;
+  if (e && cudaMemset(g_state.err, 0, sizeof(e)) != cudaSuccess) return FAS_ERR_CUDA;
+  if (f && cudaMemset(g_state.flags, 0, sizeof(f)) != cudaSuccess) return FAS_ERR_CUDA;
+  return e ? FAS_ERR_TIMEOUT : FAS_ERR_BOUND;
 }
 
 int fas_prepass_readback(float* mu, float* frame_max, float* stat, uint8_t* elig, float* row_bound,
@@ -851,6 +857,7 @@ const char* fas_error_string(int status) {
     case FAS_ERR_TIMEOUT: return "device-side wait exceeded its bound";
     case FAS_ERR_UNSUPPORTED: return "unsupported";
     case FAS_ERR_SCRATCH: return "problem larger than the fixed scratch of fas_prepass_noalloc";
+    case FAS_ERR_BOUND: return "bounded softmax sums out of range (q or k changed since the prepass?)";
     default: return "unknown status";
   }
 }

@@ -131,6 +131,9 @@ __device__ __forceinline__ void softmax_epilogue(Barriers& bars, uint32_t tmem, 
     lw += bars.red[q][1][trow];
   }
   if (!ok) return;
+  // A bound that does not hold for these q and k shows in the row's sum
+  // (see kFlagBoundRange); the row is still written, the host is told.
+  if (bounded && valid && g == 0 && !(l >= kBoundSumMin && l <= kBoundSumMax)) atomicOr(p.flags, kFlagBoundRange);
   ptx::tc_fence_after_sync();
   const float inv = 1.0f / lw;
   uint16_t* orow = p.out + (int64_t)h * p.out_head_stride + ((int64_t)sp.x + row) * p.out_row_stride;

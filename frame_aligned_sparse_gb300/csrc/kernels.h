@@ -15,6 +15,17 @@ constexpr unsigned int kErrWaitDrain = 8u;
 constexpr unsigned int kErrWaitSelftest = 16u;
 constexpr unsigned int kErrWaitPrepass = 32u;
 
+// Flag word bits (a word of its own: they report on results and stop no
+// wait).  kFlagBoundRange: a bounded row's probability sum under its bound
+// left [kBoundSumMin, kBoundSumMax].  A valid bound keeps every weight at or
+// below 1 and, for an eligible head (slack <= 32 nats), the largest at or
+// above e^-32, so the sum lies in [2^-47, keys]; outside the range the
+// weights overflowed or their largest neared fp32's subnormal range, which
+// a bound from other inputs (q or k changed after the prepass) causes.
+constexpr unsigned int kFlagBoundRange = 1u;
+constexpr float kBoundSumMin = 0x1p-100f;
+constexpr float kBoundSumMax = 0x1p100f;
+
 // Bound on any single device-side wait in the attention kernel.
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
 
@@ -71,6 +82,7 @@ struct FwdParams {
   int64_t out_head_stride; // elements
   float* lse;              // [H, N]
   unsigned int* err;       // device error word
+  unsigned int* flags;     // device word for kFlagBoundRange (never stops a wait)
   int64_t N;
   int Bk;
   int kst, vst;            // K and V ring depths (set by the launcher from the smem budget)

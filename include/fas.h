@@ -44,7 +44,8 @@
  * Argument and order checks are synchronous and leave the state unchanged.
  * Launch failures return FAS_ERR_CUDA.  A device-side wait that exceeds its
  * bound sets the device error word; the next synchronising call (fas_status,
- * or fas_prepass with elig_host) returns FAS_ERR_TIMEOUT.  No call traps or
+ * or fas_prepass with elig_host) returns FAS_ERR_TIMEOUT.  fas_status also
+ * reports FAS_ERR_BOUND (bounded softmax sums out of range, see fas_forward).  No call traps or
  * asserts on the device.
  */
 #ifndef FAS_H_
@@ -64,7 +65,8 @@ enum {
   FAS_ERR_CUDA = -4,        /* CUDA runtime/driver error (no device, launch failure) */
   FAS_ERR_TIMEOUT = -5,     /* a bounded device-side wait expired */
   FAS_ERR_UNSUPPORTED = -6, /* valid request this build does not support */
-  FAS_ERR_SCRATCH = -7      /* problem needs more than fas_prepass_noalloc's fixed scratch */
+  FAS_ERR_SCRATCH = -7,     /* problem needs more than fas_prepass_noalloc's fixed scratch */
+  FAS_ERR_BOUND = -8        /* a bounded row's softmax sum left [2^-100, 2^100] (see fas_status) */
 };
 
 enum {
@@ -163,8 +165,17 @@ int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_h
 /* Attention.  q, k, v, out: device bf16 in the current layout ([H, N, d],
  * or [N, H, d] after fas_set_layout); lse: device fp32 [H, N].  Modes AUTO
  * and BOUNDED need a prior fas_prepass on the same q and k (else
- * FAS_ERR_STATE); ONLINE does not.  Every output row is written exactly
- * once; out rows are rounded to bf16 (nearest even). */
+ * FAS_ERR_STATE); ONLINE does not.  "Same" is checked by pointer only: a
+ * caller that overwrites q or k in place must call fas_prepass again.  If
+ * it does not, the kernel still guards the result: a bounded row whose
+ * probability sum under its bound falls outside [2^-100, 2^100] (weights
+ * that overflowed, or whose largest neared fp32's subnormal range) sets a
+ * flag that the next fas_status reports as FAS_ERR_BOUND.  Inside that range
+ * the bounded softmax is accurate whatever bound it was given (the bound
+ * only shifts the exponent).  With fresh bounds an eligible head's sums lie
+ * in [2^-47, keys], so the flag never fires; BOUNDED mode on an ineligible
+ * head can fire it.  Every output row is written exactly once; out rows are
+ * rounded to bf16 (nearest even). */
 int fas_forward(const void* q, const void* k, const void* v, void* out, float* lse,
                 int mode, void* cuda_stream);
 
@@ -230,8 +241,9 @@ int fas_set_layout(int layout);
 /* Release every library-owned device buffer and forget the plan. */
 int fas_free(void);
 
-/* Synchronise the stream and report the device error word (FAS_OK or
- * FAS_ERR_TIMEOUT); clears the word. */
+/* Synchronise the stream and report the device words: FAS_ERR_TIMEOUT if a
+ * bounded wait gave up, else FAS_ERR_BOUND if a bounded row's sum left its
+ * safe range (see fas_forward), else FAS_OK; clears both words. */
 int fas_status(void* cuda_stream);
 
 /* Copy prepass results to host buffers (each nullable); synchronises the

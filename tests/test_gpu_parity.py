@@ -255,6 +255,32 @@ def test_argument_and_order_errors():
     assert fas.fas_status() == fas.FAS_OK
 
 
+
+def test_stale_bounds_are_reported():
+    """q overwritten in place after the prepass (x32, exact in bf16): the
+    pointer check cannot see it, the bounded rows' sums overflow and the next
+    fas_status reports FAS_ERR_BOUND; a fresh prepass clears it, and AUTO
+    then agrees with ONLINE on the new inputs."""
+    c = case("mid")
+    c.plan()
+    q, k = c.q.clone(), c.k.clone()
+    fas.fas_prepass(q, k)
+    out, lse = fas.fas_forward(q, k, c.v, mode="auto")
+    assert fas.fas_status() == fas.FAS_OK
+    q.mul_(32)
+    fas.fas_forward(q, k, c.v, mode="auto")
+    assert fas.fas_status() == fas.FAS_ERR_BOUND
+    assert fas.fas_status() == fas.FAS_OK  # the flag was cleared
+    elig = fas.fas_prepass(q, k, want_elig=True)
+    a_out, a_lse = fas.fas_forward(q, k, c.v, mode="auto")
+    a_out, a_lse = a_out.float(), a_lse.clone()
+    assert fas.fas_status() == fas.FAS_OK
+    o_out, o_lse = fas.fas_forward(q, k, c.v, mode="online")
+    assert fas.fas_status() == fas.FAS_OK
+    assert elig.sum() < c.w.heads  # the scaled heads lost their eligibility
+    assert (a_out - o_out.float()).abs().max().item() <= OUT_TOL
+    assert (a_lse - o_lse).abs().max().item() <= LSE_TOL
+
 def host_bf16(bits):
     return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
 

@@ -214,6 +214,7 @@ def test_calls_out_of_order_return_state_error():
     assert lib.fas_status(None) == fas.FAS_ERR_STATE
     assert lib.fas_prepass_readback(None, None, None, None, None, None) == fas.FAS_ERR_STATE
     assert lib.fas_selftest_wait_timeout(0, None) == fas.FAS_ERR_ARG
+    assert b"q or k changed" in lib.fas_error_string(fas.FAS_ERR_BOUND)
     assert lib.fas_error_string(fas.FAS_ERR_TIMEOUT).decode().startswith("device-side wait")
 
 
