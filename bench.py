@@ -70,6 +70,7 @@ def max_over_ranks(ms: float, device=None) -> float:
 def pinned_copy_gbs(host_in, host_out, dev_buf, stream):
     """GB/s of one pinned host->device copy of host_in and one device->host
     copy into host_out (each the larger of two timings), on the stream."""
+    import torch
     res = []
     for src, dst in ((host_in, dev_buf), (dev_buf, host_out)):
         best = 0.0

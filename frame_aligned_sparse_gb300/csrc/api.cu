@@ -33,8 +33,9 @@ struct State {
   float* fsum = nullptr;
   float* kmax_part = nullptr;
   float* frame_max = nullptr;
-  float* mvis = nullptr;
+  float* gmax_frame = nullptr;
   float* kbarc = nullptr;
+  float* mvis = nullptr;
   float* row_bound = nullptr;
   float* gmax_part = nullptr;
   float* stat = nullptr;
@@ -151,8 +152,9 @@ int allocate(const HostPlan& p) {
       {H * Nf * D * 4, (void**)&s.fsum},
       {H * Nf * C * 4, (void**)&s.kmax_part},
       {H * Nf * 4, (void**)&s.frame_max},
-      {H * Nf * 4, (void**)&s.mvis},
+      {H * Nf * 4, (void**)&s.gmax_frame},
       {H * Nf * D * 4, (void**)&s.kbarc},
+      {H * Nf * 4, (void**)&s.mvis},
       {H * N * 4, (void**)&s.row_bound},
       {H * Nf * C * 4, (void**)&s.gmax_part},
       {H * 4, (void**)&s.stat},
@@ -221,8 +223,9 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   a.mu = s.mu + H0 * D;
   a.fsum = s.fsum + H0 * Nf * D;
   a.frame_max = s.frame_max + H0 * Nf;
-  a.mvis = s.mvis + H0 * Nf;
+  a.gmax_frame = s.gmax_frame + H0 * Nf;
   a.kbarc = s.kbarc + H0 * Nf * D;
+  a.mvis = s.mvis + H0 * Nf;
   a.row_bound = s.row_bound + H0 * N;
   a.stat = s.stat + H0;
   a.elig = s.elig + H0;

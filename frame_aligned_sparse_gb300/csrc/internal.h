@@ -9,11 +9,12 @@ namespace fas {
 constexpr int kQTile = 128;        // query rows per work item (MMA M)
 constexpr int kMaxBlockK = 160;    // largest key block: TMEM (O, two S buffers, Q) and the softmax registers
 #ifndef FAS_PREPASS_ROWS
-#define FAS_PREPASS_ROWS 1024
+#define FAS_PREPASS_ROWS 256
 #endif
-constexpr int kPrepassRows = FAS_PREPASS_ROWS;  // rows per prepass work item, at most (items never cross frames)
+constexpr int kPrepassRows = FAS_PREPASS_ROWS;  // rows per prepass work item (one warp's), at most; items never cross frames
+constexpr int kPrepassRowsNoalloc = 1024;       // the same for fas_prepass_noalloc (fewer partial results to hold)
 #ifndef FAS_PREPASS_CTAS
-#define FAS_PREPASS_CTAS 4
+#define FAS_PREPASS_CTAS 2
 #endif
 constexpr int kPrepassCtasPerSm = FAS_PREPASS_CTAS;  // resident prepass CTAs per SM (bounds its registers)
 

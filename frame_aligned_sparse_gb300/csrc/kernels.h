@@ -48,8 +48,9 @@ struct PrepassArgs {
   float* mu;            // [H, d]              mean key
   float* fsum;          // [H, Nf, d]          per-frame key sums
   float* frame_max;     // [H, Nf]             per-frame max centred key norm
-  float* mvis;          // [H, Nf]             max over the frames visible from f
+  float* gmax_frame;    // [H, Nf]             per-frame max slack
   float* kbarc;         // [H, Nf, d]          mean centred key visible from f
+  float* mvis;          // [H, Nf]             max over the frames visible from f
   float* row_bound;     // [H, N]              m_i (natural-log units)
   float* stat;          // [H]                 max slack per head
   uint8_t* elig;        // [H]
@@ -57,7 +58,7 @@ struct PrepassArgs {
   unsigned int* err;    // device error word
   int64_t N;
   int T;                // frame span when spans is null; else the largest span
-  int Nf, H, d, chunks; // chunks: items per frame and phase
+  int Nf, H, d, chunks; // chunks: items per frame and phase (any count >= 1)
   float scale;          // 1/sqrt(d)
   uint64_t limit_ns;    // bound on each wait for another item's result
 };

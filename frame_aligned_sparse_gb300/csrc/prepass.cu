@@ -14,40 +14,44 @@
 // Since the mean of the visible centred logits is at most their maximum,
 // G_i bounds the gap between b_i and the true centred row maximum.
 //
-// One persistent kernel, four 256-thread CTAs per SM.  Work items are
-// (phase, head, frame, chunk of at most 1024 rows of that frame), taken from
-// a queue in the order
-//     keys(h)  centred(h-L)  queries(h-2L)    for h = 0, 1, ..., H+2L-1
+// One persistent kernel, one CTA of twelve warps per SM, in which every warp
+// works on its own.  A work item is (phase, head, frame, chunk of at most
+// 256 of the frame's rows) and belongs to one warp.  The warp streams the
+// rows through a private ring of shared-memory stages that bulk copies
+// (cp.async.bulk, completing on an mbarrier) fill ahead of it, running into
+// the next item's rows (input data, ready whatever the next item waits for)
+// while it works on this one, so memory parallelism is set by shared
+// memory, not registers.  No barrier spans more than a warp, so a warp
+// waiting on memory, an atomic or a flag holds up no other.  The queue
+// holds every head's items of one phase before the next phase's:
 //   keys:     column sums of the chunk's keys;
 //   centred:  max |k_j - mu_h|^2 over the chunk (needs mu_h);
-//   queries:  m_i and the max of G_i over the chunk (needs the window
-//             statistics of head h).
-// With a lag of L = 3 heads between phases, by the time a head's centred
-// (or query) items come out of the queue its keys (or centred) items have
-// finished, so items rarely wait.  Keys are first read with an evict-last
-// L2 policy and read the second time (like the queries) with evict-first,
-// so that the L heads' keys between their two reads (about 60 MB at the
-// 720p geometry) stay in L2 while the query stream passes through: K is
-// read from DRAM once, and the prepass moves one K and one Q from HBM plus
-// the small outputs.  An item's fixed costs (taking it from the queue,
-// waiting for its head's flag, the reductions and completion counts) are a
-// chain of dependent steps; four CTAs per SM run four such chains at once,
-// and large items spread each chain's cost over more bytes.
-// Completion is counted per frame and per head: the item that completes a
-// frame reduces its chunks' results, and the item that completes the last
-// frame of a head reduces the frames and publishes the next phase's inputs:
-// mu_h after the key sums (the frame sums on the way); Mvis and kbar_c
-// after the centred maxima (the frame maxima on the way); stat_h and the
-// eligibility bit after the queries.  These reductions sit on the critical
-// path of every head, so they keep many loads in flight and add in a fixed
-// order.  A consumer item polls the head's ready flag with a bounded wait.
+//   queries:  m_i and the max of G_i over the chunk (needs kbar_c and the
+//             window maximum of its frame: the warp that completes a head's
+//             keys writes every frame's kbar_c right after mu_h, the one that
+//             completes its centred maxima every frame's window maximum, and
+//             the second of the two publishes the head's ready flag).
+// An item's inputs come from a phase whose items all left the queue long
+// before, so items practically never wait; the price is that K is read
+// twice, the second time mostly from DRAM (a lag of a few heads between
+// phases kept the second read in L2 but made items wait for their head's
+// mean, which cost more).  Every read carries an evict-first L2 policy, so
+// the stream leaves L2 to the kernels around it.  Completion is
+// counted per frame and per head: the warp that completes a frame reduces
+// its chunks' results, and the warp that completes a head's last frame
+// reduces the frames.  A consumer item polls its head's ready flag with a
+// bounded wait.
 //
-// All loads are 16-byte vectors, one row shared by d/8 consecutive lanes
-// (each row's d values are contiguous), consecutive rows over the block.
-// Rows of one head are row_stride elements apart: d in the head-major
-// [H, N, d] layout, H*d in the token-major [N, H, d] layout.  Every reduction
-// runs in a fixed order (no floating-point atomics), so results are
-// bit-reproducible whichever CTA completes a phase.
+// A stage holds up to 32 rows (d = 128) or 64 rows (d = 64): one bulk copy
+// when a head's rows are contiguous (the head-major [H, N, d] layout), one
+// per row otherwise (token-major [N, H, d], rows H*d elements apart).  Four
+// lanes share a row, each with a fixed quarter of the columns (and the
+// matching quarter of mu_h and kbar_c in registers), so a row's dot
+// products and norms need two shuffle steps and the key sums none until
+// the item ends; the arithmetic runs on packed fp32 pairs (fma.rn.f32x2,
+// add.rn.f32x2), two elements per instruction.  Every reduction runs in a
+// fixed order (no floating-point atomics), so results are bit-reproducible
+// whichever warp does an item.
 
 #include <cuda_runtime.h>
 #include <math.h>
@@ -56,52 +60,75 @@
 #include "fas.h"
 #include "internal.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace fas {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kUnroll = 4;  // 16-byte loads in flight per thread in a sweep
+#ifndef FAS_PREPASS_STAGES
+#define FAS_PREPASS_STAGES 2
+#endif
+#ifndef FAS_PREPASS_WARPS
+#define FAS_PREPASS_WARPS 12
+#endif
+constexpr int kWarps = FAS_PREPASS_WARPS;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kStages = FAS_PREPASS_STAGES;  // ring stages per warp
+#ifndef FAS_PREPASS_STAGE_BYTES
+#define FAS_PREPASS_STAGE_BYTES 8192
+#endif
+constexpr int kStageBytes = FAS_PREPASS_STAGE_BYTES;
+constexpr size_t kSmemBytes = (size_t)kWarps * kStages * kStageBytes;
 
 enum Phase { kKeys = 0, kCentred = 1, kQueries = 2 };
 
-#ifndef FAS_PREPASS_LAG
-#define FAS_PREPASS_LAG 3
-#endif
-constexpr int kLag = FAS_PREPASS_LAG;  // heads between consecutive phases in the queue
 
-__device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8]) {
-  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    f[2 * e] = __uint_as_float(w[e] << 16);
-    f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-  }
+
+// Packed fp32 pairs (sm_100 family): a bf16 pair word as two fp32 lanes, and
+// lane-wise add / fused multiply-add.
+__device__ __forceinline__ uint64_t bf16_pair(uint32_t w) {
+  uint64_t r;
+  asm("{\n\t.reg .b32 lo, hi;\n\tshl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xffff0000;\n\tmov.b64 %0, {lo, hi};\n\t}"
+      : "=l"(r) : "r"(w));
+  return r;
 }
-
-// 16-byte load through L2 with an L2 eviction policy, not kept in L1 (each
-// row is read once per phase).
-__device__ __forceinline__ uint4 ld_policy(const uint4* p, uint64_t policy) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p), "l"(policy));
+__device__ __forceinline__ uint64_t pair(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpair(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 
-// Keys' first read: keep the line in L2 ahead of other lines (its second
-// read comes L heads later).
-__device__ __forceinline__ uint64_t evict_last_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
 
-// A line's last use (keys' second read, queries): first to leave L2.
+// Streamed lines (K twice, Q once; none is reused from L2 in time): first to
+// leave L2.
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to this CTA's shared memory, completing on the mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -114,77 +141,70 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait (one thread) for a ready flag.  Gives up at once when the
+// Bounded wait (one lane) for a ready flag.  Gives up at once when the
 // error word is already set, or after limit_ns, recording kErrWaitPrepass.
 __device__ bool wait_ready(const unsigned* flag, unsigned* err, uint64_t limit_ns) {
   if (ld_acquire(flag)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t t0 = ptx::global_timer_ns();
   for (;;) {
-    __nanosleep(100);
+    __nanosleep(200);
     if (ld_acquire(flag)) return true;
     if (*reinterpret_cast<volatile unsigned*>(err) != 0u) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
+    if (ptx::global_timer_ns() - t0 > limit_ns) {
       atomicOr(err, kErrWaitPrepass);
       return false;
     }
   }
 }
 
-// Block-wide max of one float per thread.
-__device__ __forceinline__ float block_max(float v, float* scratch) {
+// Bounded wait (every lane) for a ring stage's copies.  The waiting warp
+// sleeps in the try-wait (a suspend-time hint) rather than spinning, so it
+// leaves its scheduler's issue slots to the other warps.  With `give_up`,
+// it returns false once the error word is set (the caller then drains).
+__device__ bool stage_wait(uint32_t bar, uint32_t parity, unsigned* err, uint64_t limit_ns, bool give_up) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (;;) {
+    if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (give_up && *reinterpret_cast<volatile unsigned*>(err) != 0u) return false;
+    if (ptx::global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, kErrWaitPrepass);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  __syncthreads();  // scratch may still be read from the previous call
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  float r = scratch[0];
-  for (int w = 1; w < kThreads / 32; ++w) r = fmaxf(r, scratch[w]);
-  return r;
+  return v;
 }
 
-constexpr int kCacheFrames = kThreads / 8;  // frames whose sums fit in `red` for the window statistics
-
-struct Shared {
-  float red[kThreads / 8][128];  // per-row-slot column sums; later the head's frame sums
-  float fmax[kCacheFrames];      // the head's frame maxima
-  float scratch[kThreads / 32];
-  int item;
-  int last;
-  int ok;
-};
-
-// Sum of p[i * stride] for i = 0 .. n-1, added in index order, with eight
-// loads in flight (data written by other CTAs of this launch: read at L2).
-__device__ __forceinline__ float ordered_sum(const float* p, int n, int64_t stride) {
-  float s = 0.f;
-  for (int i = 0; i < n; i += 8) {
-    float v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = i + u < n ? __ldcg(p + (int64_t)(i + u) * stride) : 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) s += v[u];  // adding the 0 of a missing element leaves s exact
-  }
-  return s;
-}
-
-// Maximum of p[i] for i = 0 .. n-1 (order-free: max is exact), at least lo.
-__device__ __forceinline__ float batched_max(const float* p, int n, float lo) {
+// Maximum of p[0 .. n-1] over the warp (order-free: max is exact), at least lo.
+__device__ __forceinline__ float warp_max_of(const float* p, int n, float lo, int lane) {
   float m = lo;
+  for (int i = lane; i < n; i += 32) m = fmaxf(m, __ldcg(p + i));
+  return warp_max(m);
+}
+
+// s[e] = sum over i < n of p[i * stride + e], e < CPL, added in index order,
+// with eight rows of loads in flight (data written by other warps of this
+// launch: read at L2).
+template <int CPL>
+__device__ __forceinline__ void ordered_sum(const float* p, int n, int64_t stride, float (&s)[CPL]) {
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) s[e] = 0.f;
   for (int i = 0; i < n; i += 8) {
-    float v[8];
+    float v[8][CPL];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = i + u < n ? __ldcg(p + i + u) : lo;
+    for (int u = 0; u < 8; ++u)
 #pragma unroll
-    for (int u = 0; u < 8; ++u) m = fmaxf(m, v[u]);
+      for (int e = 0; e < CPL; ++e) v[u][e] = i + u < n ? __ldcg(p + (int64_t)(i + u) * stride + e) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) s[e] += v[u][e];  // adding the 0 of a missing row leaves s exact
   }
-  return m;
 }
 
 // Visible frames of query frame f: [a0, a1) and [b0, b1).
@@ -198,257 +218,456 @@ __device__ __forceinline__ int2 span(const PrepassArgs& a, int g) {
   return a.spans ? a.spans[g] : make_int2(g * a.T, a.T);
 }
 
-// Signals that this CTA finished its item of (phase, head); returns true in
-// the CTA that finished the last one (all threads).  Every thread's global
-// writes of the item are made visible before the count.
-__device__ __forceinline__ bool finish_item(unsigned* done, int n_items, Shared& sh) {
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(done, 1u);
-    sh.last = old == (unsigned)(n_items - 1);
-    if (sh.last) __threadfence();
-  }
-  __syncthreads();
-  return sh.last != 0;
+// Segment j (0 <= j < 3H) of the queue: {phase, head}.  The queue holds
+// every head's key items, then every head's centred items, then every
+// head's query items: an item's inputs come from items two or more
+// segments (hundreds of items) earlier, finished long before it is taken.
+__device__ __forceinline__ int2 segment(int j, int H) { return make_int2(j / H, j % H); }
+
+struct Item {
+  int phase, h, g, row0, rows;
+  int64_t hf, pi;  // per-frame and per-item slots
+};
+
+__device__ __forceinline__ Item decode(const PrepassArgs& a, int item) {
+  const int per = a.Nf * a.chunks;
+  const int2 seg = segment(item / per, a.H);
+  const int local = item % per;
+  Item it;
+  it.phase = seg.x;
+  it.h = seg.y;
+  it.g = local / a.chunks;
+  const int c = local % a.chunks;
+  const int2 sp = span(a, it.g);
+  it.row0 = sp.x + (int)(((int64_t)sp.y * c) / a.chunks);
+  it.rows = sp.x + (int)(((int64_t)sp.y * (c + 1)) / a.chunks) - it.row0;
+  it.hf = (int64_t)it.h * a.Nf + it.g;
+  it.pi = it.hf * a.chunks + c;
+  return it;
 }
 
-// Publishes a ready flag once every thread's writes are visible.
-__device__ __forceinline__ void publish(unsigned* flag) {
+// Counts the warp's item of a group of n; true (all lanes) in the warp that
+// counted the last one.  Every lane's writes of the item are made visible
+// before the count, and the last warp's reads come after it.
+__device__ __forceinline__ bool warp_finish(unsigned* done, int n, int lane) {
   __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) st_release(flag, 1u);
+  __syncwarp();
+  unsigned last = 0;
+  if (lane == 0) last = atomicAdd(done, 1u) == (unsigned)(n - 1);
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) __threadfence();
+  return last != 0;
 }
+
+// Publishes a ready flag once every lane's writes are visible.
+__device__ __forceinline__ void warp_publish(unsigned* flag, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) st_release(flag, 1u);
+}
+
+// One of the two results a head's query items wait for is written (the
+// window mean centred keys, or the window maxima); the second to arrive
+// publishes the ready flag.
+__device__ __forceinline__ void win_arrive(unsigned* count, unsigned* flag, int lane) {
+  __threadfence();
+  __syncwarp();
+  unsigned second = 0;
+  if (lane == 0) second = atomicAdd(count, 1u) == 1u;
+  if (__shfl_sync(0xffffffffu, second, 0)) {
+    __threadfence();
+    if (lane == 0) st_release(flag, 1u);
+  }
+}
+
+// v[e] = p[e], e < N (N = 2 or 4), one vector load from L2.
+template <int N>
+__device__ __forceinline__ void load_cols(const float* p, float (&v)[N]) {
+  if constexpr (N == 4) {
+    const float4 t = __ldcg(reinterpret_cast<const float4*>(p));
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  } else {
+    const float2 t = __ldcg(reinterpret_cast<const float2*>(p));
+    v[0] = t.x, v[1] = t.y;
+  }
+}
+
+// One warp's ring of shared-memory stages, filled and emptied in order.
+template <int D>
+struct Ring {
+  static constexpr int kRowBytes = 2 * D;
+  static constexpr int kRowsPerStage = kStageBytes / kRowBytes;  // 32 (d = 128) or 64 (d = 64)
+  uint32_t buf;  // this warp's first stage (shared address)
+  uint32_t bar;  // this warp's first stage barrier (shared address)
+  unsigned issued, consumed;
+
+  __device__ __forceinline__ uint32_t stage_buf(unsigned n) const { return buf + (n % kStages) * kStageBytes; }
+  __device__ __forceinline__ uint32_t stage_bar(unsigned n) const { return bar + (n % kStages) * 8; }
+
+  static __device__ __forceinline__ int stages(const Item& it) { return (it.rows + kRowsPerStage - 1) / kRowsPerStage; }
+
+  // Copies stage t of the item (its rows t*kRowsPerStage ..) into the next
+  // slot.  Warp-wide.
+  __device__ __forceinline__ void issue(const PrepassArgs& a, const Item& it, int t, int lane, uint64_t pol) {
+    const int r0 = t * kRowsPerStage;
+    const int n = min(kRowsPerStage, it.rows - r0);
+    const uint16_t* src = static_cast<const uint16_t*>(it.phase == kQueries ? a.q : a.k) +
+                          (int64_t)it.h * a.head_stride + (int64_t)(it.row0 + r0) * a.row_stride;
+    const uint32_t dst = stage_buf(issued), b = stage_bar(issued);
+    if (lane == 0) ptx::mbar_arrive_expect_tx(b, (uint32_t)(n * kRowBytes));
+    if (a.row_stride == D) {
+      if (lane == 0) bulk_g2s(dst, src, (uint32_t)(n * kRowBytes), b, pol);
+    } else {
+      __syncwarp();  // the expected byte count is set before any copy lands
+      for (int i = lane; i < n; i += 32)
+        bulk_g2s(dst + (uint32_t)(i * kRowBytes), src + (int64_t)i * a.row_stride, kRowBytes, b, pol);
+    }
+    ++issued;
+  }
+};
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, kPrepassCtasPerSm) prepass_kernel(const PrepassArgs a) {
-  constexpr int VPR = D / 8;              // 16-byte vectors per row
-  constexpr int RPI = kThreads / VPR;     // rows per sweep
-  __shared__ Shared sh;
-  const int v = threadIdx.x % VPR, rs = threadIdx.x / VPR;
+__global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs a) {
+  using R = Ring<D>;
+  constexpr int VPR = D / 8;                   // 16-byte chunks per row
+  constexpr int NCH = D / 32;                  // chunks per lane: four lanes share a row
+  constexpr int STEPS = R::kRowsPerStage / 8;  // eight rows per warp-wide read
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t bars[kWarps][kStages];
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  // Lane (rl, sg) reads rows rl, rl + 8, ... of a stage and, of each, the
+  // chunks sg + 4 (j ^ x), j < NCH, x = rl & 1: its columns are fixed, and
+  // the eight lanes of each quarter-warp read eight different bank groups.
+  const int sg = lane & 3, rl = lane >> 2, xr = rl & 1;
+  int chunk[NCH];
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) chunk[j] = sg + 4 * (j ^ xr);
   const int H = a.H, Nf = a.Nf, C = a.chunks;
-  const int per = Nf * C;                 // items per (phase, head)
-  const int total = 3 * (H + 2 * kLag) * per;
+  const int total = 3 * H * Nf * C;
   unsigned* const queue = a.sync;
-  unsigned* const keys_frame_done = a.sync + 1;           // [H, Nf] items done per frame
+  unsigned* const keys_frame_done = a.sync + 1;  // [H, Nf] items done per frame and phase
   unsigned* const cent_frame_done = keys_frame_done + H * Nf;
-  unsigned* const keys_done = cent_frame_done + H * Nf;   // [H] frames done per head
+  unsigned* const qry_frame_done = cent_frame_done + H * Nf;
+  unsigned* const keys_done = qry_frame_done + H * Nf;  // [H] frames done per head and phase
   unsigned* const cent_done = keys_done + H;
-  unsigned* const qry_done = cent_done + H;                // [H] items done per head
+  unsigned* const qry_done = cent_done + H;
   unsigned* const mu_ready = qry_done + H;
   unsigned* const win_ready = mu_ready + H;
-  const uint4* const q = static_cast<const uint4*>(a.q);
-  const uint4* const k = static_cast<const uint4*>(a.k);
-  const int64_t rstride = a.row_stride / 8, hstride = a.head_stride / 8;  // in 16-byte vectors
-  const uint64_t last_use = evict_first_policy();
-  const uint64_t reused = evict_last_policy();
+  unsigned* const win_count = win_ready + H;  // [H] of the two window results written
+  const uint64_t drop = evict_first_policy();  // every read is the line's last use in this kernel
+  const uint32_t smem_base = ptx::smem_addr(smem);
 
-  for (;;) {
-    if (threadIdx.x == 0) {
-      sh.item = (*reinterpret_cast<volatile unsigned*>(a.err) != 0u) ? total : (int)atomicAdd(queue, 1u);
-      sh.ok = 1;
-    }
-    __syncthreads();
-    const int item = sh.item;
-    __syncthreads();
-    if (item >= total) break;
-    const int seg = item / per, local = item % per;
-    const int phase = seg % 3, h = seg / 3 - kLag * phase;
-    if (h < 0 || h >= H) continue;  // the queue's first and last steps have fewer phases
-    const int g = local / C, c = local % C;
-    const int2 sp = span(a, g);
-    const int row0 = sp.x + (int)(((int64_t)sp.y * c) / C);
-    const int rows = sp.x + (int)(((int64_t)sp.y * (c + 1)) / C) - row0;
-    const int64_t pi = ((int64_t)h * Nf + g) * C + c;  // per-item slot
+  R ring;
+  ring.buf = smem_base + (uint32_t)(warp * kStages * kStageBytes);
+  ring.bar = ptx::smem_addr(&bars[warp][0]);
+  ring.issued = ring.consumed = 0;
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) ptx::mbar_init(ring.bar + s * 8, 1);
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  __syncwarp();
 
-    if (phase != kKeys) {
-      if (threadIdx.x == 0) sh.ok = wait_ready(phase == kCentred ? &mu_ready[h] : &win_ready[h], a.err, a.limit_ns);
-      __syncthreads();
-      const int ok = sh.ok;
-      __syncthreads();  // every thread has read the flag before thread 0 may rewrite it
-      if (!ok) continue;  // the error word is set; the loop drains the queue
-    }
+  // Item A is worked on; item B is the next one, whose index is fetched
+  // while A runs and whose rows enter the ring once A's are all issued.
+  unsigned raw = 0;
+  if (lane == 0) raw = atomicAdd(queue, 1u);
+  const int ia = (int)__shfl_sync(0xffffffffu, raw, 0);
+  if (ia < total) {
+    Item A = decode(a, ia), B = A;
+    int nA = R::stages(A), tA = 0, nB = 0, tB = 0;
+    unsigned rawB = 0;
+    if (lane == 0) rawB = atomicAdd(queue, 1u);
+    int ib = -1;        // B's index, once looked at
+    bool hasB = false;  // B decoded
+    // Keeps every stage of the ring in flight: A's remaining rows, then B's.
+    auto top_up = [&]() {
+      while (ring.issued - ring.consumed < (unsigned)kStages) {
+        if (tA < nA) {
+          ring.issue(a, A, tA++, lane, drop);
+          continue;
+        }
+        if (ib < 0) ib = (int)__shfl_sync(0xffffffffu, rawB, 0);
+        if (ib >= total) break;
+        if (!hasB) {
+          B = decode(a, ib);
+          nB = R::stages(B);
+          tB = 0;
+          hasB = true;
+        }
+        if (tB >= nB) break;
+        ring.issue(a, B, tB++, lane, drop);
+      }
+    };
 
-    if (phase == kKeys) {
-      // Column sums of the chunk's keys.
-      const uint4* base = k + (int64_t)h * hstride + (int64_t)row0 * rstride + v;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      int r = rs;
-      for (; r + 3 * RPI < rows; r += 4 * RPI) {
-        uint4 x[4];
+    for (;;) {
+      top_up();
+      if (A.phase != kKeys) {
+        unsigned got = 1;
+        if (lane == 0) got = wait_ready(A.phase == kCentred ? &mu_ready[A.h] : &win_ready[A.h], a.err, a.limit_ns);
+        if (!__shfl_sync(0xffffffffu, got, 0)) break;  // the error word is set; drain below
+      }
+      const int64_t hbase = (int64_t)A.h * D;
+      float acc[NCH][8], m[NCH][8], kb[NCH][8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) x[u] = ld_policy(base + (int64_t)(r + u * RPI) * rstride, reused);
+      for (int j = 0; j < NCH; ++j)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float f[8];
-          unpack8(x[u], f);
+        for (int e = 0; e < 8; ++e) acc[j][e] = m[j][e] = kb[j][e] = 0.f;
+      float best = 0.f, gmax = -INFINITY, Mv = 0.f;
+      if (A.phase != kKeys) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] += f[e];
+        for (int j = 0; j < NCH; ++j) {
+          const float4* mp = reinterpret_cast<const float4*>(a.mu + hbase + chunk[j] * 8);
+          const float4 lo = __ldcg(mp), hi = __ldcg(mp + 1);
+          m[j][0] = lo.x, m[j][1] = lo.y, m[j][2] = lo.z, m[j][3] = lo.w;
+          m[j][4] = hi.x, m[j][5] = hi.y, m[j][6] = hi.z, m[j][7] = hi.w;
         }
       }
-      for (; r < rows; r += RPI) {
-        float f[8];
-        unpack8(ld_policy(base + (int64_t)r * rstride, reused), f);
+      if (A.phase == kQueries) {
+        // The frame's window statistics (written once per frame when the
+        // head's keys and centred maxima completed).
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += f[e];
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sh.red[rs][v * 8 + e] = acc[e];
-      __syncthreads();
-      if (threadIdx.x < D) {
-        float s = 0.f;
-        for (int t = 0; t < RPI; ++t) s += sh.red[t][threadIdx.x];
-        a.ksum_part[pi * D + threadIdx.x] = s;
-      }
-      if (finish_item(&keys_frame_done[h * Nf + g], C, sh)) {
-        // The frame's key sums, in chunk order.
-        if (threadIdx.x < D)
-          a.fsum[((int64_t)h * Nf + g) * D + threadIdx.x] =
-              ordered_sum(&a.ksum_part[((int64_t)h * Nf + g) * C * D + threadIdx.x], C, D);
-        if (finish_item(&keys_done[h], Nf, sh)) {
-          // The head's mean key, from the frame sums in frame order.
-          if (threadIdx.x < D)
-            a.mu[(int64_t)h * D + threadIdx.x] =
-                ordered_sum(&a.fsum[(int64_t)h * Nf * D + threadIdx.x], Nf, D) / (float)a.N;
-          publish(&mu_ready[h]);
+        for (int j = 0; j < NCH; ++j) {
+          const float4* kp = reinterpret_cast<const float4*>(a.kbarc + A.hf * D + chunk[j] * 8);
+          const float4 lo = __ldcg(kp), hi = __ldcg(kp + 1);
+          kb[j][0] = lo.x, kb[j][1] = lo.y, kb[j][2] = lo.z, kb[j][3] = lo.w;
+          kb[j][4] = hi.x, kb[j][5] = hi.y, kb[j][6] = hi.z, kb[j][7] = hi.w;
         }
+        Mv = __ldcg(&a.mvis[A.hf]);
       }
-    } else if (phase == kCentred) {
-      // Largest |k_j - mu_h|^2 over the chunk.
-      float m[8];
+      float* const out = a.row_bound + (int64_t)A.h * a.N + A.row0;
+      uint64_t acc2[NCH][4], m2[NCH][4], negm2[NCH][4], kb2[NCH][4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m[e] = __ldcg(&a.mu[(int64_t)h * D + v * 8 + e]);
-      const uint4* base = k + (int64_t)h * hstride + (int64_t)row0 * rstride + v;
-      float best = 0.f;
-      // Uniform trip count across the block so the lane shuffles stay converged.
-      for (int r0 = 0; r0 < rows; r0 += kUnroll * RPI) {
-        uint4 x[kUnroll];
+      for (int j = 0; j < NCH; ++j)
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int r = r0 + u * RPI + rs;
-          x[u] = r < rows ? ld_policy(base + (int64_t)r * rstride, last_use) : make_uint4(0, 0, 0, 0);
+        for (int e = 0; e < 4; ++e) {
+          acc2[j][e] = 0;
+          m2[j][e] = pair(m[j][2 * e], m[j][2 * e + 1]);
+          negm2[j][e] = pair(-m[j][2 * e], -m[j][2 * e + 1]);
+          kb2[j][e] = pair(kb[j][2 * e], kb[j][2 * e + 1]);
         }
+
+      bool ok = true;
+      for (int t = 0; t < nA; ++t) {
+        top_up();
+        const unsigned n_st = ring.consumed;
+        if (!stage_wait(ring.stage_bar(n_st), (n_st / kStages) & 1u, a.err, a.limit_ns, true)) {
+          ok = false;
+          break;
+        }
+        const uint4* sb = reinterpret_cast<const uint4*>(smem + (ring.stage_buf(n_st) - smem_base));
+        const int r0 = t * R::kRowsPerStage;
+        const int n = min(R::kRowsPerStage, A.rows - r0);
+        if (A.phase == kKeys) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int r = r0 + u * RPI + rs;
-          float f[8];
-          unpack8(x[u], f);
-          float s = 0.f;
+          for (int q = 0; q < STEPS; ++q) {
+            const int row = q * 8 + rl;
+            if (row < n) {
+#pragma unroll
+              for (int j = 0; j < NCH; ++j) {
+                const uint4 x = sb[row * VPR + chunk[j]];
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc2[j][e] = add2(acc2[j][e], bf16_pair(w[e]));
+              }
+            }
+          }
+        } else if (A.phase == kCentred) {
+#pragma unroll
+          for (int q = 0; q < STEPS; ++q) {
+            const int row = q * 8 + rl;
+            const bool valid = row < n;
+            uint64_t s2 = 0;
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+              const uint4 x = valid ? sb[row * VPR + chunk[j]] : make_uint4(0, 0, 0, 0);
+              const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const uint64_t dlt = add2(bf16_pair(w[e]), negm2[j][e]);
+                fma2(s2, dlt, dlt);
+              }
+            }
+            const float2 sp2 = unpair(s2);
+            float s = sp2.x + sp2.y;
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (valid) best = fmaxf(best, s);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < STEPS; ++q) {
+            const int row = q * 8 + rl;
+            const bool valid = row < n;
+            uint64_t qq2 = 0, qm2 = 0, qk2 = 0;
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+              const uint4 x = valid ? sb[row * VPR + chunk[j]] : make_uint4(0, 0, 0, 0);
+              const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const uint64_t f2 = bf16_pair(w[e]);
+                fma2(qq2, f2, f2);
+                fma2(qm2, f2, m2[j][e]);
+                fma2(qk2, f2, kb2[j][e]);
+              }
+            }
+            const float2 a2 = unpair(qq2), b2 = unpair(qm2), c2 = unpair(qk2);
+            float qq = a2.x + a2.y, qm = b2.x + b2.y, qk = c2.x + c2.y;
+            qq += __shfl_xor_sync(0xffffffffu, qq, 1);
+            qm += __shfl_xor_sync(0xffffffffu, qm, 1);
+            qk += __shfl_xor_sync(0xffffffffu, qk, 1);
+            qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+            qm += __shfl_xor_sync(0xffffffffu, qm, 2);
+            qk += __shfl_xor_sync(0xffffffffu, qk, 2);
+            if (valid && sg == 0) {
+              const float b = a.scale * sqrtf(qq) * Mv;
+              out[r0 + row] = fmaf(a.scale, qm, b);
+              gmax = fmaxf(gmax, b - a.scale * qk);
+            }
+          }
+        }
+        // The stage's shared-memory reads (generic proxy) are ordered
+        // before the bulk copy that refills it (async proxy).
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        ++ring.consumed;
+      }
+      if (!ok) break;
+
+      if (A.phase == kKeys) {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 t2 = unpair(acc2[j][e]);
+            acc[j][2 * e] = t2.x;
+            acc[j][2 * e + 1] = t2.y;
+          }
+        // Column sums: first every lane's sums in chunk order sg + 4j (the
+        // odd rows' lanes read the chunk pairs swapped), then the eight
+        // row lanes of each column group added in a fixed tree.
+#pragma unroll
+        for (int j = 0; j < NCH; j += 2)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float t = f[e] - m[e];
-            s = fmaf(t, t, s);
+            const float u0 = acc[j][e], u1 = acc[j + 1][e];
+            acc[j][e] = xr ? u1 : u0;
+            acc[j + 1][e] = xr ? u0 : u1;
           }
 #pragma unroll
-          for (int o = VPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (r < rows) best = fmaxf(best, s);
+        for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+          for (int j = 0; j < NCH; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j][e] += __shfl_xor_sync(0xffffffffu, acc[j][e], o);
+        if (rl == 0) {
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            float4* dst = reinterpret_cast<float4*>(a.ksum_part + A.pi * D + (sg + 4 * j) * 8);
+            dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+            dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+          }
         }
-      }
-      const float bm = block_max(best, sh.scratch);
-      if (threadIdx.x == 0) a.kmax_part[pi] = bm;
-      if (finish_item(&cent_frame_done[h * Nf + g], C, sh)) {
-        if (threadIdx.x == 0)
-          a.frame_max[(int64_t)h * Nf + g] = sqrtf(batched_max(&a.kmax_part[((int64_t)h * Nf + g) * C], C, 0.f));
-        if (finish_item(&cent_done[h], Nf, sh)) {
-          // Per query frame: the max of the visible frames' maxima and the
-          // mean centred key over the visible keys (frame sums added in
-          // frame order).  The head's frame sums and maxima are staged in
-          // shared memory first when they fit.
-          const bool cached = Nf <= kCacheFrames;
-          if (cached) {
-            if (threadIdx.x < D)
-              for (int g0 = 0; g0 < Nf; g0 += 8) {
-                float v[8];
+        if (warp_finish(&keys_frame_done[A.hf], C, lane)) {
+          // The frame's key sums, in chunk order.
+          constexpr int CPL = D / 32;
+          float s[CPL];
+          ordered_sum<CPL>(a.ksum_part + A.hf * C * D + lane * CPL, C, D, s);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  v[u] = g0 + u < Nf ? __ldcg(&a.fsum[((int64_t)h * Nf + g0 + u) * D + threadIdx.x]) : 0.f;
+          for (int e = 0; e < CPL; ++e) a.fsum[A.hf * D + lane * CPL + e] = s[e];
+          if (warp_finish(&keys_done[A.h], Nf, lane)) {
+            // The head's mean key, from the frame sums in frame order.
+            ordered_sum<CPL>(a.fsum + (int64_t)A.h * Nf * D + lane * CPL, Nf, D, s);
+            float mu_l[CPL];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  if (g0 + u < Nf) sh.red[g0 + u][threadIdx.x] = v[u];
-              }
-            for (int gg = threadIdx.x; gg < Nf; gg += kThreads) sh.fmax[gg] = __ldcg(&a.frame_max[(int64_t)h * Nf + gg]);
-          }
-          __syncthreads();
-          if (threadIdx.x < D) {
-            const int e = threadIdx.x;
-            const float mue = __ldcg(&a.mu[(int64_t)h * D + e]);
+            for (int e = 0; e < CPL; ++e) {
+              mu_l[e] = s[e] / (float)a.N;
+              a.mu[hbase + lane * CPL + e] = mu_l[e];
+            }
+            warp_publish(&mu_ready[A.h], lane);
+            // Per query frame: the mean centred key over the keys it sees
+            // (frame sums added in frame order).
             for (int f = 0; f < Nf; ++f) {
               const int4 vis = visible(a, f);
-              float acc = 0.f, mx = 0.f;
+              float kc[CPL];
+#pragma unroll
+              for (int e = 0; e < CPL; ++e) kc[e] = 0.f;
               int64_t cnt = 0;
+#pragma unroll
               for (int part = 0; part < 2; ++part) {
                 const int g0 = part == 0 ? vis.x : vis.z, g1 = part == 0 ? vis.y : vis.w;
                 for (int gg = g0; gg < g1; ++gg) {
-                  acc += cached ? sh.red[gg][e] : __ldcg(&a.fsum[((int64_t)h * Nf + gg) * D + e]);
-                  mx = fmaxf(mx, cached ? sh.fmax[gg] : __ldcg(&a.frame_max[(int64_t)h * Nf + gg]));
+                  float fv[CPL];
+                  load_cols<CPL>(a.fsum + ((int64_t)A.h * Nf + gg) * D + lane * CPL, fv);
+#pragma unroll
+                  for (int e = 0; e < CPL; ++e) kc[e] += fv[e];
                   cnt += span(a, gg).y;
                 }
               }
-              a.kbarc[((int64_t)h * Nf + f) * D + e] = acc / (float)cnt - mue;
-              if (e == 0) a.mvis[(int64_t)h * Nf + f] = mx;
+#pragma unroll
+              for (int e = 0; e < CPL; ++e)
+                a.kbarc[((int64_t)A.h * Nf + f) * D + lane * CPL + e] = kc[e] / (float)cnt - mu_l[e];
+            }
+            win_arrive(&win_count[A.h], &win_ready[A.h], lane);
+          }
+        }
+      } else if (A.phase == kCentred) {
+        best = warp_max(best);
+        if (lane == 0) a.kmax_part[A.pi] = best;
+        if (warp_finish(&cent_frame_done[A.hf], C, lane)) {
+          const float mx = warp_max_of(a.kmax_part + A.hf * C, C, 0.f, lane);
+          if (lane == 0) a.frame_max[A.hf] = sqrtf(mx);
+          if (warp_finish(&cent_done[A.h], Nf, lane)) {
+            // Per query frame: the largest maximum of the frames it sees.
+            for (int f = lane; f < Nf; f += 32) {
+              const int4 vis = visible(a, f);
+              float mx = 0.f;
+              for (int gg = vis.x; gg < vis.y; ++gg) mx = fmaxf(mx, __ldcg(&a.frame_max[(int64_t)A.h * Nf + gg]));
+              for (int gg = vis.z; gg < vis.w; ++gg) mx = fmaxf(mx, __ldcg(&a.frame_max[(int64_t)A.h * Nf + gg]));
+              a.mvis[(int64_t)A.h * Nf + f] = mx;
+            }
+            win_arrive(&win_count[A.h], &win_ready[A.h], lane);
+          }
+        }
+      } else {
+        gmax = warp_max(gmax);
+        if (lane == 0) a.gmax_part[A.pi] = gmax;
+        if (warp_finish(&qry_frame_done[A.hf], C, lane)) {
+          const float fm = warp_max_of(a.gmax_part + A.hf * C, C, -INFINITY, lane);
+          if (lane == 0) a.gmax_frame[A.hf] = fm;
+          if (warp_finish(&qry_done[A.h], Nf, lane)) {
+            // Largest slack of the head (max is exact in any order).
+            const float mx = warp_max_of(a.gmax_frame + (int64_t)A.h * Nf, Nf, -INFINITY, lane);
+            if (lane == 0) {
+              a.stat[A.h] = mx;
+              a.elig[A.h] = mx <= FAS_ELIG_SLACK_NATS ? 1 : 0;
             }
           }
-          publish(&win_ready[h]);
         }
       }
-    } else {
-      // Row bounds and the chunk's largest slack.
-      float m[8], kb[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        m[e] = __ldcg(&a.mu[(int64_t)h * D + v * 8 + e]);
-        kb[e] = __ldcg(&a.kbarc[((int64_t)h * Nf + g) * D + v * 8 + e]);
+
+      // Next item: B (whose first stages may already be in the ring).
+      if (ib < 0) ib = (int)__shfl_sync(0xffffffffu, rawB, 0);
+      if (ib >= total) break;
+      if (!hasB) {
+        B = decode(a, ib);
+        nB = R::stages(B);
+        tB = 0;
       }
-      const float Mv = __ldcg(&a.mvis[(int64_t)h * Nf + g]);
-      const uint4* base = q + (int64_t)h * hstride + (int64_t)row0 * rstride + v;
-      float* out = a.row_bound + (int64_t)h * a.N + row0;
-      float gmax = -INFINITY;
-      for (int r0 = 0; r0 < rows; r0 += kUnroll * RPI) {
-        uint4 x[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int r = r0 + u * RPI + rs;
-          x[u] = r < rows ? ld_policy(base + (int64_t)r * rstride, last_use) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int r = r0 + u * RPI + rs;
-          float f[8];
-          unpack8(x[u], f);
-          float qq = 0.f, qm = 0.f, qk = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            qq = fmaf(f[e], f[e], qq);
-            qm = fmaf(f[e], m[e], qm);
-            qk = fmaf(f[e], kb[e], qk);
-          }
-#pragma unroll
-          for (int o = VPR / 2; o > 0; o >>= 1) {
-            qq += __shfl_xor_sync(0xffffffffu, qq, o);
-            qm += __shfl_xor_sync(0xffffffffu, qm, o);
-            qk += __shfl_xor_sync(0xffffffffu, qk, o);
-          }
-          if (r < rows && v == 0) {
-            const float b = a.scale * sqrtf(qq) * Mv;
-            out[r] = fmaf(a.scale, qm, b);
-            gmax = fmaxf(gmax, b - a.scale * qk);
-          }
-        }
-      }
-      const float bm = block_max(gmax, sh.scratch);
-      if (threadIdx.x == 0) a.gmax_part[pi] = bm;
-      if (finish_item(&qry_done[h], per, sh)) {
-        // Largest slack of the head over all its items (max is exact in any
-        // order), with every thread loading.
-        float mx = -INFINITY;
-        for (int i = threadIdx.x; i < per; i += kThreads) mx = fmaxf(mx, __ldcg(&a.gmax_part[(int64_t)h * per + i]));
-        mx = block_max(mx, sh.scratch);
-        if (threadIdx.x == 0) {
-          a.stat[h] = mx;
-          a.elig[h] = mx <= FAS_ELIG_SLACK_NATS ? 1 : 0;
-        }
-      }
+      A = B;
+      nA = nB;
+      tA = tB;
+      hasB = false;
+      ib = -1;
+      if (lane == 0) rawB = atomicAdd(queue, 1u);
     }
+  }
+  // Copies still in flight land before the warp leaves (after a failure; on
+  // the normal path every issued stage has been consumed).
+  while (ring.consumed < ring.issued) {
+    stage_wait(ring.stage_bar(ring.consumed), (ring.consumed / kStages) & 1u, a.err, a.limit_ns, false);
+    ++ring.consumed;
   }
 }
 
@@ -461,13 +680,18 @@ int grid_size(int items) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepass_kernel<D>, kThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1, sms = sms > 0 ? sms : 1;
-    if (per_sm > kPrepassCtasPerSm) per_sm = kPrepassCtasPerSm;
+        cudaFuncSetAttribute(prepass_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepass_kernel<D>, kThreads, kSmemBytes) !=
+            cudaSuccess ||
+        per_sm < 1) {
+      per_sm = 0;
+      return -1;
+    }
   }
   const int g = per_sm * sms;
-  return g < items ? g : items;
+  const int need = (items + kWarps - 1) / kWarps;  // one item per warp at least
+  return g < need ? g : need;
 }
 
 template <int D>
@@ -477,15 +701,17 @@ int launch_d(const PrepassArgs& a, cudaStream_t st) {
   // gives up on a wait leaves every head on the safe path.
   if (cudaMemsetAsync(a.sync, 0, prepass_sync_words(a.H, a.Nf) * sizeof(unsigned), st) != cudaSuccess) return -1;
   if (cudaMemsetAsync(a.elig, 0, (size_t)a.H, st) != cudaSuccess) return -1;
-  const int items = 3 * (a.H + 2 * kLag) * a.Nf * a.chunks;
-  prepass_kernel<D><<<grid_size<D>(items), kThreads, 0, st>>>(a);
+  const int items = 3 * a.H * a.Nf * a.chunks;
+  const int grid = grid_size<D>(items);
+  if (grid < 1) return -1;
+  prepass_kernel<D><<<grid, kThreads, kSmemBytes, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return -1;
   return 1;
 }
 
 }  // namespace
 
-size_t prepass_sync_words(int H, int Nf) { return 1 + 2 * (size_t)H * Nf + 5 * (size_t)H; }
+size_t prepass_sync_words(int H, int Nf) { return 1 + 3 * (size_t)H * Nf + 6 * (size_t)H; }
 
 int launch_prepass(const PrepassArgs& a, cudaStream_t stream) {
   if (a.d == 128) return launch_d<128>(a, stream);

@@ -81,12 +81,14 @@ extern "C" int fas_prepass_noalloc(const void* q, const void* k, int frame_token
     return FAS_ERR_ALIGN;
 
   // Scratch layout: per-item key sums, per-item centred maxima, per-item
-  // slack maxima, mean key, frame sums, frame maxima, window maxima, window
-  // mean centred keys (fp32), then the counters and flags and the error word.
-  const int chunks = (T + kPrepassRows - 1) / kPrepassRows;
+  // slack maxima, mean key, frame sums, frame maxima, frame slack maxima,
+  // window mean centred keys, window maxima (fp32), then the counters and
+  // flags and the error word.
+  const int chunks = (T + kPrepassRowsNoalloc - 1) / kPrepassRowsNoalloc;
   const size_t hs = (size_t)H, nf = (size_t)Nf, cs = (size_t)chunks, ds = (size_t)d;
-  const size_t sizes[10] = {hs * nf * cs * ds * 4, hs * nf * cs * 4, hs * nf * cs * 4, hs * ds * 4,
-                            hs * nf * ds * 4,      hs * nf * 4,      hs * nf * 4,      hs * nf * ds * 4,
+  const size_t sizes[11] = {hs * nf * cs * ds * 4, hs * nf * cs * 4, hs * nf * cs * 4,
+                            hs * ds * 4,           hs * nf * ds * 4, hs * nf * 4,
+                            hs * nf * 4,           hs * nf * ds * 4, hs * nf * 4,
                             prepass_sync_words(H, (int)Nf) * 4, 4};
   size_t total = 0;
   for (size_t b : sizes) total += round256(b);
@@ -95,9 +97,9 @@ extern "C" int fas_prepass_noalloc(const void* q, const void* k, int frame_token
   void* base = nullptr;
   const int rc = scratch_address(&base);
   if (rc != FAS_OK) return rc;
-  void* part[10];
+  void* part[11];
   size_t off = 0;
-  for (int i = 0; i < 10; ++i) {
+  for (int i = 0; i < 11; ++i) {
     part[i] = static_cast<unsigned char*>(base) + off;
     off += round256(sizes[i]);
   }
@@ -117,10 +119,11 @@ extern "C" int fas_prepass_noalloc(const void* q, const void* k, int frame_token
   a.mu = static_cast<float*>(part[3]);
   a.fsum = static_cast<float*>(part[4]);
   a.frame_max = static_cast<float*>(part[5]);
-  a.mvis = static_cast<float*>(part[6]);
+  a.gmax_frame = static_cast<float*>(part[6]);
   a.kbarc = static_cast<float*>(part[7]);
-  a.sync = static_cast<unsigned int*>(part[8]);
-  a.err = static_cast<unsigned int*>(part[9]);
+  a.mvis = static_cast<float*>(part[8]);
+  a.sync = static_cast<unsigned int*>(part[9]);
+  a.err = static_cast<unsigned int*>(part[10]);
   a.row_bound = row_bound;
   a.stat = stat;
   a.elig = elig;

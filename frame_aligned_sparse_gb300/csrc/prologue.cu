@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       // Producer: fill f goes to stage f % S after the stage's previous fill
       // is consumed by the MMAs of every CTA of the cluster (and, for
       // first-tile fills, by this CTA's row sums).
+      // x (each panel read once per column tile) and W' (read by every
+      // panel of the part) stay in L2 ahead of the q, k, v stream.
+      const uint64_t keep = ptx::policy_evict_last();
       int fill = 0;
       bool ok = true;
       for (int n = 0; ok && n < ncol; ++n)
@@ -157,12 +160,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           const uint32_t dst = ring + s * kStageBytes;
           const uint32_t fb = ptx::smem_addr(&bars.full[s]);
           ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-          ptx::tma_load_2d(dst, &tm_x, fb, kk * kKStep, panel * kRows);
+          ptx::tma_load_2d_hint(dst, &tm_x, fb, kk * kKStep, panel * kRows, keep);
           if (CL == 1)
-            ptx::tma_load_2d(dst + kABytes, &tm_w, fb, kk * kKStep, part * p.heads * D + n * TN);
+            ptx::tma_load_2d_hint(dst + kABytes, &tm_w, fb, kk * kKStep, part * p.heads * D + n * TN, keep);
           else
-            ptx::tma_load_2d_multicast(dst + kABytes + rank * (kBBytes / CL), &tm_w, fb, kk * kKStep,
-                                       part * p.heads * D + n * TN + (int)rank * (TN / CL), kMask);
+            ptx::tma_load_2d_multicast_hint(dst + kABytes + rank * (kBBytes / CL), &tm_w, fb, kk * kKStep,
+                                            part * p.heads * D + n * TN + (int)rank * (TN / CL), kMask, keep);
         }
       if (!ok) {
         // Let the copies already started land before the CTA exits (a
@@ -231,7 +234,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const uint4* src = reinterpret_cast<const uint4*>(ring_ptr + s * kStageBytes + row * 128);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint4 v = src[c];
+        // The row's eight pieces in the order of the swizzled rows' bank
+        // groups, so that eight consecutive rows read eight different ones.
+        const uint4 v = src[c ^ (row & 7)];
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -248,6 +253,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       ptx::mbar_arrive(ptx::smem_addr(&bars.rowsum[s]));
     }
     const float rstd = rsqrtf((ss0 + ss1) / (float)p.width + p.eps);
+    const uint64_t stream = ptx::policy_evict_first();  // q, k, v: written once here, read by later kernels
     uint16_t* const out = static_cast<uint16_t*>(part == 0 ? p.q : part == 1 ? p.k : p.v);
     const float* const ctab = p.cos_tab + (valid ? token : 0) * (D / 2);
     const float* const stab = p.sin_tab + (valid ? token : 0) * (D / 2);
@@ -303,10 +309,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             }
             uint4* d0 = reinterpret_cast<uint4*>(dst + c * 16);
             uint4* d1 = reinterpret_cast<uint4*>(dst + D / 2 + c * 16);
-            d0[0] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-            d0[1] = make_uint4(pl[4], pl[5], pl[6], pl[7]);
-            d1[0] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-            d1[1] = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+            ptx::st_global_hint(d0, make_uint4(pl[0], pl[1], pl[2], pl[3]), stream);
+            ptx::st_global_hint(d0 + 1, make_uint4(pl[4], pl[5], pl[6], pl[7]), stream);
+            ptx::st_global_hint(d1, make_uint4(ph[0], ph[1], ph[2], ph[3]), stream);
+            ptx::st_global_hint(d1 + 1, make_uint4(ph[4], ph[5], ph[6], ph[7]), stream);
           }
         }
       }

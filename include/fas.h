@@ -279,9 +279,9 @@ int fas_selftest_wait_timeout(int limit_us, void* cuda_stream);
  *   stat       : device fp32 [H], receives stat_h;
  *   elig       : device uint8 [H], receives the eligibility bits.
  * The geometry arguments follow fas_plan.  The scratch needed is about
- * 4 * H * Nf * (ceil(T/1024) * d + 2 * d) bytes; a geometry that does not
- * fit returns FAS_ERR_SCRATCH before any device work (e.g. 720p and 1080p SR
- * chunks with H up to 48, d = 128 fit; H = 64 at 720p does not).
+ * 4 * H * Nf * (ceil(T/1024) * d + 2 * d) bytes; a geometry that does not fit
+ * returns FAS_ERR_SCRATCH before any device work (e.g. 720p and 1080p SR
+ * chunks with H up to 48, d = 128 fit; H = 96 at 720p does not).
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current, and again after the
  * device's context has changed (a device reset); make that first call

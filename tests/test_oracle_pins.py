@@ -501,7 +501,7 @@ def test_bound_on_mid_sampled_rows():
 
 
 VISIBLE_FLOPS_TFLOP = {"tiny": 4.6e-5, "mid": 0.679, "720p": 22.61, "1080p": 52.37, "stress": 22.61, "dense": 77.08,
-                       "720p_h4": 22.61 * 4 / 24}
+                       "720p_h4": 22.61 * 4 / 24, "720p_f5": 4.778}
 
 
 def test_visible_flops_per_workload():

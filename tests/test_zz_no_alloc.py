@@ -102,11 +102,11 @@ def test_noalloc_prepass_edge_geometries(lib, spec):
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch(lib):
-    # 64 heads of the 720p geometry need about 4.4 MB of scratch (> 4 MiB).
+    # 96 heads of the 720p geometry need about 5.6 MB of scratch (> 4 MiB).
     q = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(16, device="cuda")
     elig = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    rc = lib.fas_prepass_noalloc(q.data_ptr(), q.data_ptr(), 3600, 21, 1, 2, 64, 128, out.data_ptr(),
+    rc = lib.fas_prepass_noalloc(q.data_ptr(), q.data_ptr(), 3600, 21, 1, 2, 96, 128, out.data_ptr(),
                                  out.data_ptr(), elig.data_ptr(), None)
     assert rc == fas.FAS_ERR_SCRATCH
     assert "fixed scratch" in lib.fas_error_string(rc).decode()

@@ -90,6 +90,10 @@ WORKLOADS: Dict[str, Workload] = {
         # The 720p geometry with 4 heads (0.24 GB of Q/K/V, still larger than
         # L2): small enough for multi-pass profiler captures.
         Workload("720p_h4", 4, 128, 1, 21, 3600, 2, 3.0, 5),
+        # The 720p heads and frames with 5 video frames (21,600 tokens): the
+        # prologue's full 3072-wide projection over ~3.4 waves of CTAs in a
+        # few GB, for multi-pass profiler captures.
+        Workload("720p_f5", 24, 128, 1, 5, 3600, 2, 3.0, 6),
     ]
 }
 
@@ -187,7 +191,7 @@ def generate(w: Workload | str,
 
 #: Latent grid width (patches per row) of each workload's frames: the frame
 #: span T is grid_w x (T / grid_w) patches.
-GRID_W = {"tiny": 8, "mid": 40, "720p": 80, "1080p": 120, "stress": 80, "dense": 80, "720p_h4": 80}
+GRID_W = {"tiny": 8, "mid": 40, "720p": 80, "1080p": 120, "stress": 80, "dense": 80, "720p_h4": 80, "720p_f5": 80}
 
 
 def rotary_tables(w: Workload, grid_w: Optional[int] = None, base: float = 10000.0):
