@@ -14,7 +14,7 @@
 // Since the mean of the visible centred logits is at most their maximum,
 // G_i bounds the gap between b_i and the true centred row maximum.
 //
-// One persistent kernel, one CTA of twelve warps per SM, in which every warp
+// One persistent kernel, one CTA of sixteen warps per SM, in which every warp
 // works on its own.  A work item is (phase, head, frame, chunk of at most
 // 256 of the frame's rows) and belongs to one warp.  The warp streams the
 // rows through a private ring of shared-memory stages that bulk copies
@@ -42,9 +42,11 @@
 // reduces the frames.  A consumer item polls its head's ready flag with a
 // bounded wait.
 //
-// A stage holds up to 32 rows (d = 128) or 64 rows (d = 64): one bulk copy
-// when a head's rows are contiguous (the head-major [H, N, d] layout), one
-// per row otherwise (token-major [N, H, d], rows H*d elements apart).  Four
+// A stage (6 KB; two per warp) holds up to 24 rows (d = 128) or 48 rows
+// (d = 64): one bulk copy when a head's rows are contiguous (the head-major
+// [H, N, d] layout), one per row otherwise (token-major [N, H, d], rows H*d
+// elements apart).  Each phase keeps only its own registers (126 at most),
+// so sixteen warps fit on an SM.  Four
 // lanes share a row, each with a fixed quarter of the columns (and the
 // matching quarter of mu_h and kbar_c in registers), so a row's dot
 // products and norms need two shuffle steps and the key sums none until
@@ -69,13 +71,13 @@ namespace {
 #define FAS_PREPASS_STAGES 2
 #endif
 #ifndef FAS_PREPASS_WARPS
-#define FAS_PREPASS_WARPS 12
+#define FAS_PREPASS_WARPS 16
 #endif
 constexpr int kWarps = FAS_PREPASS_WARPS;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = FAS_PREPASS_STAGES;  // ring stages per warp
 #ifndef FAS_PREPASS_STAGE_BYTES
-#define FAS_PREPASS_STAGE_BYTES 8192
+#define FAS_PREPASS_STAGE_BYTES 6144
 #endif
 constexpr int kStageBytes = FAS_PREPASS_STAGE_BYTES;
 constexpr size_t kSmemBytes = (size_t)kWarps * kStages * kStageBytes;
@@ -408,134 +410,62 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
         if (!__shfl_sync(0xffffffffu, got, 0)) break;  // the error word is set; drain below
       }
       const int64_t hbase = (int64_t)A.h * D;
-      float acc[NCH][8], m[NCH][8], kb[NCH][8];
-#pragma unroll
-      for (int j = 0; j < NCH; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] = m[j][e] = kb[j][e] = 0.f;
-      float best = 0.f, gmax = -INFINITY, Mv = 0.f;
-      if (A.phase != kKeys) {
+      // Streams the item's stages, body(sb, r0, n) on each (sb: the stage's
+      // rows, r0: its first row in the item, n: its rows); false when a
+      // wait gave up.  Each phase below keeps its own registers.
+      auto stream_item = [&](auto&& body) -> bool {
+        for (int t = 0; t < nA; ++t) {
+          top_up();
+          const unsigned n_st = ring.consumed;
+          if (!stage_wait(ring.stage_bar(n_st), (n_st / kStages) & 1u, a.err, a.limit_ns, true)) return false;
+          const uint4* sb = reinterpret_cast<const uint4*>(smem + (ring.stage_buf(n_st) - smem_base));
+          const int r0 = t * R::kRowsPerStage;
+          body(sb, r0, min(R::kRowsPerStage, A.rows - r0));
+          // The stage's shared-memory reads (generic proxy) are ordered
+          // before the bulk copy that refills it (async proxy).
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          ++ring.consumed;
+        }
+        return true;
+      };
+      // This lane's quarter of a head-length vector, as packed pairs.
+      auto load_pairs = [&](const float* v, uint64_t (&out)[NCH][4], float sign) {
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          const float4* mp = reinterpret_cast<const float4*>(a.mu + hbase + chunk[j] * 8);
-          const float4 lo = __ldcg(mp), hi = __ldcg(mp + 1);
-          m[j][0] = lo.x, m[j][1] = lo.y, m[j][2] = lo.z, m[j][3] = lo.w;
-          m[j][4] = hi.x, m[j][5] = hi.y, m[j][6] = hi.z, m[j][7] = hi.w;
+          const float4* vp = reinterpret_cast<const float4*>(v + chunk[j] * 8);
+          const float4 lo = __ldcg(vp), hi = __ldcg(vp + 1);
+          out[j][0] = pair(sign * lo.x, sign * lo.y);
+          out[j][1] = pair(sign * lo.z, sign * lo.w);
+          out[j][2] = pair(sign * hi.x, sign * hi.y);
+          out[j][3] = pair(sign * hi.z, sign * hi.w);
         }
-      }
-      if (A.phase == kQueries) {
-        // The frame's window statistics (written once per frame when the
-        // head's keys and centred maxima completed).
-#pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-          const float4* kp = reinterpret_cast<const float4*>(a.kbarc + A.hf * D + chunk[j] * 8);
-          const float4 lo = __ldcg(kp), hi = __ldcg(kp + 1);
-          kb[j][0] = lo.x, kb[j][1] = lo.y, kb[j][2] = lo.z, kb[j][3] = lo.w;
-          kb[j][4] = hi.x, kb[j][5] = hi.y, kb[j][6] = hi.z, kb[j][7] = hi.w;
-        }
-        Mv = __ldcg(&a.mvis[A.hf]);
-      }
-      float* const out = a.row_bound + (int64_t)A.h * a.N + A.row0;
-      uint64_t acc2[NCH][4], m2[NCH][4], negm2[NCH][4], kb2[NCH][4];
-#pragma unroll
-      for (int j = 0; j < NCH; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc2[j][e] = 0;
-          m2[j][e] = pair(m[j][2 * e], m[j][2 * e + 1]);
-          negm2[j][e] = pair(-m[j][2 * e], -m[j][2 * e + 1]);
-          kb2[j][e] = pair(kb[j][2 * e], kb[j][2 * e + 1]);
-        }
-
-      bool ok = true;
-      for (int t = 0; t < nA; ++t) {
-        top_up();
-        const unsigned n_st = ring.consumed;
-        if (!stage_wait(ring.stage_bar(n_st), (n_st / kStages) & 1u, a.err, a.limit_ns, true)) {
-          ok = false;
-          break;
-        }
-        const uint4* sb = reinterpret_cast<const uint4*>(smem + (ring.stage_buf(n_st) - smem_base));
-        const int r0 = t * R::kRowsPerStage;
-        const int n = min(R::kRowsPerStage, A.rows - r0);
-        if (A.phase == kKeys) {
-#pragma unroll
-          for (int q = 0; q < STEPS; ++q) {
-            const int row = q * 8 + rl;
-            if (row < n) {
-#pragma unroll
-              for (int j = 0; j < NCH; ++j) {
-                const uint4 x = sb[row * VPR + chunk[j]];
-                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc2[j][e] = add2(acc2[j][e], bf16_pair(w[e]));
-              }
-            }
-          }
-        } else if (A.phase == kCentred) {
-#pragma unroll
-          for (int q = 0; q < STEPS; ++q) {
-            const int row = q * 8 + rl;
-            const bool valid = row < n;
-            uint64_t s2 = 0;
-#pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-              const uint4 x = valid ? sb[row * VPR + chunk[j]] : make_uint4(0, 0, 0, 0);
-              const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const uint64_t dlt = add2(bf16_pair(w[e]), negm2[j][e]);
-                fma2(s2, dlt, dlt);
-              }
-            }
-            const float2 sp2 = unpair(s2);
-            float s = sp2.x + sp2.y;
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (valid) best = fmaxf(best, s);
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < STEPS; ++q) {
-            const int row = q * 8 + rl;
-            const bool valid = row < n;
-            uint64_t qq2 = 0, qm2 = 0, qk2 = 0;
-#pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-              const uint4 x = valid ? sb[row * VPR + chunk[j]] : make_uint4(0, 0, 0, 0);
-              const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const uint64_t f2 = bf16_pair(w[e]);
-                fma2(qq2, f2, f2);
-                fma2(qm2, f2, m2[j][e]);
-                fma2(qk2, f2, kb2[j][e]);
-              }
-            }
-            const float2 a2 = unpair(qq2), b2 = unpair(qm2), c2 = unpair(qk2);
-            float qq = a2.x + a2.y, qm = b2.x + b2.y, qk = c2.x + c2.y;
-            qq += __shfl_xor_sync(0xffffffffu, qq, 1);
-            qm += __shfl_xor_sync(0xffffffffu, qm, 1);
-            qk += __shfl_xor_sync(0xffffffffu, qk, 1);
-            qq += __shfl_xor_sync(0xffffffffu, qq, 2);
-            qm += __shfl_xor_sync(0xffffffffu, qm, 2);
-            qk += __shfl_xor_sync(0xffffffffu, qk, 2);
-            if (valid && sg == 0) {
-              const float b = a.scale * sqrtf(qq) * Mv;
-              out[r0 + row] = fmaf(a.scale, qm, b);
-              gmax = fmaxf(gmax, b - a.scale * qk);
-            }
-          }
-        }
-        // The stage's shared-memory reads (generic proxy) are ordered
-        // before the bulk copy that refills it (async proxy).
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        ++ring.consumed;
-      }
-      if (!ok) break;
+      };
 
       if (A.phase == kKeys) {
+        // Column sums of the chunk's keys.
+        uint64_t acc2[NCH][4];
+#pragma unroll
+        for (int j = 0; j < NCH; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc2[j][e] = 0;
+        if (!stream_item([&](const uint4* sb, int, int n) {
+#pragma unroll
+              for (int q = 0; q < STEPS; ++q) {
+                const int row = q * 8 + rl;
+                if (row < n) {
+#pragma unroll
+                  for (int j = 0; j < NCH; ++j) {
+                    const uint4 x = sb[row * VPR + chunk[j]];
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc2[j][e] = add2(acc2[j][e], bf16_pair(w[e]));
+                  }
+                }
+              }
+            }))
+          break;
+        float acc[NCH][8];
 #pragma unroll
         for (int j = 0; j < NCH; ++j)
 #pragma unroll
@@ -544,9 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
             acc[j][2 * e] = t2.x;
             acc[j][2 * e + 1] = t2.y;
           }
-        // Column sums: first every lane's sums in chunk order sg + 4j (the
-        // odd rows' lanes read the chunk pairs swapped), then the eight
-        // row lanes of each column group added in a fixed tree.
+        // Every lane's sums in chunk order sg + 4j (the odd rows' lanes read
+        // the chunk pairs swapped), then the eight row lanes of each column
+        // group added in a fixed tree.
 #pragma unroll
         for (int j = 0; j < NCH; j += 2)
 #pragma unroll
@@ -613,6 +543,34 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
           }
         }
       } else if (A.phase == kCentred) {
+        // Largest |k_j - mu_h|^2 over the chunk.
+        uint64_t negm2[NCH][4];
+        load_pairs(a.mu + hbase, negm2, -1.f);
+        float best = 0.f;
+        if (!stream_item([&](const uint4* sb, int, int n) {
+#pragma unroll
+              for (int q = 0; q < STEPS; ++q) {
+                const int row = q * 8 + rl;
+                const bool valid = row < n;
+                uint64_t s2 = 0;
+#pragma unroll
+                for (int j = 0; j < NCH; ++j) {
+                  const uint4 x = valid ? sb[row * VPR + chunk[j]] : make_uint4(0, 0, 0, 0);
+                  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const uint64_t dlt = add2(bf16_pair(w[e]), negm2[j][e]);
+                    fma2(s2, dlt, dlt);
+                  }
+                }
+                const float2 sp2 = unpair(s2);
+                float s = sp2.x + sp2.y;
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (valid) best = fmaxf(best, s);
+              }
+            }))
+          break;
         best = warp_max(best);
         if (lane == 0) a.kmax_part[A.pi] = best;
         if (warp_finish(&cent_frame_done[A.hf], C, lane)) {
@@ -622,15 +580,58 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
             // Per query frame: the largest maximum of the frames it sees.
             for (int f = lane; f < Nf; f += 32) {
               const int4 vis = visible(a, f);
-              float mx = 0.f;
-              for (int gg = vis.x; gg < vis.y; ++gg) mx = fmaxf(mx, __ldcg(&a.frame_max[(int64_t)A.h * Nf + gg]));
-              for (int gg = vis.z; gg < vis.w; ++gg) mx = fmaxf(mx, __ldcg(&a.frame_max[(int64_t)A.h * Nf + gg]));
-              a.mvis[(int64_t)A.h * Nf + f] = mx;
+              float mx2 = 0.f;
+              for (int gg = vis.x; gg < vis.y; ++gg) mx2 = fmaxf(mx2, __ldcg(&a.frame_max[(int64_t)A.h * Nf + gg]));
+              for (int gg = vis.z; gg < vis.w; ++gg) mx2 = fmaxf(mx2, __ldcg(&a.frame_max[(int64_t)A.h * Nf + gg]));
+              a.mvis[(int64_t)A.h * Nf + f] = mx2;
             }
             win_arrive(&win_count[A.h], &win_ready[A.h], lane);
           }
         }
       } else {
+        // Row bounds and the chunk's largest slack, with the frame's window
+        // statistics (written once per frame when the head's keys and
+        // centred maxima completed).
+        uint64_t m2[NCH][4], kb2[NCH][4];
+        load_pairs(a.mu + hbase, m2, 1.f);
+        load_pairs(a.kbarc + A.hf * D, kb2, 1.f);
+        const float Mv = __ldcg(&a.mvis[A.hf]);
+        float* const out = a.row_bound + (int64_t)A.h * a.N + A.row0;
+        float gmax = -INFINITY;
+        if (!stream_item([&](const uint4* sb, int r0, int n) {
+#pragma unroll
+              for (int q = 0; q < STEPS; ++q) {
+                const int row = q * 8 + rl;
+                const bool valid = row < n;
+                uint64_t qq2 = 0, qm2 = 0, qk2 = 0;
+#pragma unroll
+                for (int j = 0; j < NCH; ++j) {
+                  const uint4 x = valid ? sb[row * VPR + chunk[j]] : make_uint4(0, 0, 0, 0);
+                  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const uint64_t f2 = bf16_pair(w[e]);
+                    fma2(qq2, f2, f2);
+                    fma2(qm2, f2, m2[j][e]);
+                    fma2(qk2, f2, kb2[j][e]);
+                  }
+                }
+                const float2 a2 = unpair(qq2), b2 = unpair(qm2), c2 = unpair(qk2);
+                float qq = a2.x + a2.y, qm = b2.x + b2.y, qk = c2.x + c2.y;
+                qq += __shfl_xor_sync(0xffffffffu, qq, 1);
+                qm += __shfl_xor_sync(0xffffffffu, qm, 1);
+                qk += __shfl_xor_sync(0xffffffffu, qk, 1);
+                qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+                qm += __shfl_xor_sync(0xffffffffu, qm, 2);
+                qk += __shfl_xor_sync(0xffffffffu, qk, 2);
+                if (valid && sg == 0) {
+                  const float b = a.scale * sqrtf(qq) * Mv;
+                  out[r0 + row] = fmaf(a.scale, qm, b);
+                  gmax = fmaxf(gmax, b - a.scale * qk);
+                }
+              }
+            }))
+          break;
         gmax = warp_max(gmax);
         if (lane == 0) a.gmax_part[A.pi] = gmax;
         if (warp_finish(&qry_frame_done[A.hf], C, lane)) {
