@@ -460,7 +460,8 @@ def run_fas(args, w):
                "achieved": pflops / (pro_ms * 1e-3) / 1e12, "peak": peak, "unit": "TFLOP/s",
                "frac": pflops / (pro_ms * 1e-3) / 1e12 / peak, "flops": pflops,
                "shape": f"x [{N}, {H * d}] -> q, k, v ({args.layout}), projection {H * d} -> {3 * H * d}",
-               "step_with_prologue_ms": chain_ms, "launches_timed": n_pro}
+               "step_with_prologue_ms": chain_ms, "launches_timed": n_pro,
+               "traffic": recorded_traffic("prologue_qkv", w.name)}
         del px, pw, wf, qkv
 
     abl = None
