@@ -23,6 +23,9 @@ struct State {
   bool planned = false;
   HostPlan plan;
   int device = -1;
+  int sms = 0;            // SMs of the plan's device
+  int chunks_k = 0;       // prepass key items per frame (fixed per plan: the frame sums' order)
+  size_t part_items = 0;  // per-item slots of the prepass's centred and query partials (the largest launch)
   void* arena = nullptr;
   int4* work = nullptr;
   int4* table = nullptr;
@@ -136,27 +139,42 @@ void release() {
 
 // Carves the library's device buffers out of one allocation.
 int allocate(const HostPlan& p) {
-  const size_t H = p.H, Nf = p.Nf, D = p.d, C = p.chunks, N = (size_t)p.N;
+  const size_t H = p.H, Nf = p.Nf, D = p.d, N = (size_t)p.N;
+  State& s = g_state;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FAS_ERR_CUDA;
+  // The key items per frame follow the plan (so the frame sums, added in
+  // chunk order, are the same in every launch); a launch over nh heads
+  // holds nh * Nf * chunks(nh) centred and query partials, and the host
+  // pipeline launches over head groups of any size up to H.
+  s.chunks_k = fas::prepass_chunks(p.H, p.N, p.T, s.sms);
+  s.part_items = 0;
+  for (int nh = 1; nh <= p.H; ++nh) {
+    const size_t items = (size_t)nh * Nf * fas::prepass_chunks(nh, p.N, p.T, s.sms);
+    if (items > s.part_items) s.part_items = items;
+  }
+  const size_t PI = s.part_items;
   struct Part {
     size_t bytes;
     void** dst;
   };
-  State& s = g_state;
   Part parts[] = {
       {(size_t)p.n_work * sizeof(int4), (void**)&s.work},
       {Nf * sizeof(int4), (void**)&s.table},
       {Nf * sizeof(int2), (void**)&s.spans},
       {Nf * sizeof(int4), (void**)&s.fvis},
-      {H * Nf * C * D * 4, (void**)&s.ksum_part},
+      {H * Nf * (size_t)s.chunks_k * D * 4, (void**)&s.ksum_part},
       {H * D * 4, (void**)&s.mu},
       {H * Nf * D * 4, (void**)&s.fsum},
-      {H * Nf * C * 4, (void**)&s.kmax_part},
+      {PI * 4, (void**)&s.kmax_part},
       {H * Nf * 4, (void**)&s.frame_max},
       {H * Nf * 4, (void**)&s.gmax_frame},
       {H * Nf * D * 4, (void**)&s.kbarc},
       {H * Nf * 4, (void**)&s.mvis},
       {H * N * 4, (void**)&s.row_bound},
-      {H * Nf * C * 4, (void**)&s.gmax_part},
+      {PI * 4, (void**)&s.gmax_part},
       {H * 4, (void**)&s.stat},
       {H, (void**)&s.elig},
       {fas::prepass_sync_words(p.H, p.Nf) * 4, (void**)&s.sync},
@@ -203,11 +221,12 @@ int64_t head_stride() {
 }
 
 // Prepass arguments for heads [h0, h0 + nh) of q and k (every per-head
-// statistics buffer is head-major, so it is offset by h0).
+// statistics buffer is head-major, so it is offset by h0; the per-item
+// partial results are the launch's own scratch, from the start).
 fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   const HostPlan& p = g_state.plan;
   State& s = g_state;
-  const size_t H0 = (size_t)h0, Nf = p.Nf, D = p.d, C = p.chunks, N = (size_t)p.N;
+  const size_t H0 = (size_t)h0, Nf = p.Nf, D = p.d, N = (size_t)p.N;
   fas::PrepassArgs a;
   a.q = static_cast<const uint16_t*>(q) + h0 * head_stride();
   a.k = static_cast<const uint16_t*>(k) + h0 * head_stride();
@@ -217,9 +236,9 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   a.fvis = s.fvis;
   a.R0 = p.R0;
   a.r = p.r;
-  a.ksum_part = s.ksum_part + H0 * Nf * C * D;
-  a.kmax_part = s.kmax_part + H0 * Nf * C;
-  a.gmax_part = s.gmax_part + H0 * Nf * C;
+  a.ksum_part = s.ksum_part;  // launches run one at a time (one stream)
+  a.kmax_part = s.kmax_part;
+  a.gmax_part = s.gmax_part;
   a.mu = s.mu + H0 * D;
   a.fsum = s.fsum + H0 * Nf * D;
   a.frame_max = s.frame_max + H0 * Nf;
@@ -236,7 +255,8 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   a.Nf = p.Nf;
   a.H = nh;
   a.d = p.d;
-  a.chunks = p.chunks;
+  a.chunks_k = s.chunks_k;
+  a.chunks_q = fas::prepass_chunks(nh, p.N, p.T, s.sms);
   a.scale = (float)(1.0 / sqrt((double)p.d));
   a.limit_ns = fas::kWaitLimitNs;
   return a;

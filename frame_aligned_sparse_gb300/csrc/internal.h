@@ -12,7 +12,11 @@ constexpr int kMaxBlockK = 160;    // largest key block: TMEM (O, two S buffers,
 #define FAS_PREPASS_ROWS 256
 #endif
 constexpr int kPrepassRows = FAS_PREPASS_ROWS;  // rows per prepass work item (one warp's), at most; items never cross frames
-constexpr int kPrepassRowsNoalloc = 1024;       // the same for fas_prepass_noalloc (fewer partial results to hold)
+#ifndef FAS_PREPASS_MIN_ROWS
+#define FAS_PREPASS_MIN_ROWS 32
+#endif
+constexpr int kPrepassMinRows = FAS_PREPASS_MIN_ROWS;  // rows per prepass work item, at least (launches over few heads)
+constexpr int kPrepassRowsNoalloc = 1024;       // rows per item of fas_prepass_noalloc (fewer partial results to hold)
 #ifndef FAS_PREPASS_CTAS
 #define FAS_PREPASS_CTAS 2
 #endif
@@ -25,7 +29,6 @@ struct HostPlan {
   int64_t N = 0;
   int Bk = 0;
   int n_work = 0;
-  int chunks = 0;  // prepass items per frame and phase
   int64_t key_blocks = 0;
   double visible_flops = 0.0;
   std::vector<int32_t> spans;  // Nf x 2: first token, tokens

@@ -42,9 +42,9 @@ struct PrepassArgs {
   const int2* spans;    // [Nf] {first token, tokens} of each frame; null: frame g is [g*T, (g+1)*T)
   const int4* fvis;     // [Nf] frames visible from f: [x, y) and [z, w); null: the frame rule with R0, r
   int R0, r;            // reference frames and window radius (used when fvis is null)
-  float* ksum_part;     // [H, Nf, chunks, d]  per-item key column sums
-  float* kmax_part;     // [H, Nf, chunks]     per-item max |k - mu|^2
-  float* gmax_part;     // [H, Nf, chunks]     per-item max slack
+  float* ksum_part;     // [H, Nf, chunks_k, d] per-item key column sums
+  float* kmax_part;     // [H, Nf, chunks_q]    per-item max |k - mu|^2
+  float* gmax_part;     // [H, Nf, chunks_q]    per-item max slack
   float* mu;            // [H, d]              mean key
   float* fsum;          // [H, Nf, d]          per-frame key sums
   float* frame_max;     // [H, Nf]             per-frame max centred key norm
@@ -58,13 +58,21 @@ struct PrepassArgs {
   unsigned int* err;    // device error word
   int64_t N;
   int T;                // frame span when spans is null; else the largest span
-  int Nf, H, d, chunks; // chunks: items per frame and phase (any count >= 1)
+  int Nf, H, d;
+  int chunks_k;         // key items per frame (sets the frame sums' order: fixed per plan)
+  int chunks_q;         // centred and query items per frame (any count >= 1)
   float scale;          // 1/sqrt(d)
   uint64_t limit_ns;    // bound on each wait for another item's result
 };
 
 // 32-bit words of the prepass's counters and ready flags for H heads.
 size_t prepass_sync_words(int H, int Nf);
+
+// Work items per frame and phase for a prepass launch over `heads` heads of
+// `rows_per_head` rows (frames of at most `span_max` rows) on `sms` SMs:
+// items of kPrepassMinRows .. kPrepassRows rows, about one per two warps of
+// the launch per phase, so that a launch over few heads still spreads.
+int prepass_chunks(int heads, int64_t rows_per_head, int span_max, int sms);
 
 // Zeroes the counters and the eligibility bits, then launches the fused
 // prepass kernel on `stream`; returns the number of kernels launched (1),

@@ -56,7 +56,6 @@ int build_plan(const int32_t* spans, int T, int F, int R0, int r, int H, int d, 
 
   p.T = tmax; p.F = F; p.R0 = R0; p.r = r; p.H = H; p.d = d;
   p.Nf = (int)Nf; p.N = N; p.Bk = Bk;
-  p.chunks = (tmax + kPrepassRows - 1) / kPrepassRows;
   p.table.assign((size_t)Nf * 4, 0);
   p.fvis.assign((size_t)Nf * 4, 0);
   auto start = [&](int64_t f) -> int32_t { return f < Nf ? p.spans[(size_t)f * 2] : (int32_t)N; };

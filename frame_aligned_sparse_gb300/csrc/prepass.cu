@@ -220,31 +220,40 @@ __device__ __forceinline__ int2 span(const PrepassArgs& a, int g) {
   return a.spans ? a.spans[g] : make_int2(g * a.T, a.T);
 }
 
-// Segment j (0 <= j < 3H) of the queue: {phase, head}.  The queue holds
-// every head's key items, then every head's centred items, then every
-// head's query items: an item's inputs come from items two or more
-// segments (hundreds of items) earlier, finished long before it is taken.
-__device__ __forceinline__ int2 segment(int j, int H) { return make_int2(j / H, j % H); }
-
 struct Item {
   int phase, h, g, row0, rows;
+  int C;           // items per frame of the item's phase
   int64_t hf, pi;  // per-frame and per-item slots
 };
 
+// Item `item` of the queue: every head's key items (chunks_k per frame),
+// then every head's centred items, then every head's query items
+// (chunks_q per frame each), heads and frames in order.  An item's inputs
+// come from a phase whose items all left the queue long before it.
 __device__ __forceinline__ Item decode(const PrepassArgs& a, int item) {
-  const int per = a.Nf * a.chunks;
-  const int2 seg = segment(item / per, a.H);
-  const int local = item % per;
+  const int nk = a.H * a.Nf * a.chunks_k, nq = a.H * a.Nf * a.chunks_q;
   Item it;
-  it.phase = seg.x;
-  it.h = seg.y;
-  it.g = local / a.chunks;
-  const int c = local % a.chunks;
+  int local;
+  if (item < nk) {
+    it.phase = kKeys, it.C = a.chunks_k, local = item;
+  } else if (item < nk + nq) {
+    it.phase = kCentred, it.C = a.chunks_q, local = item - nk;
+  } else {
+    it.phase = kQueries, it.C = a.chunks_q, local = item - nk - nq;
+  }
+  const int per = a.Nf * it.C;
+  it.h = local / per;
+  it.g = (local % per) / it.C;
+  const int c = local % it.C;
+  // Chunk boundaries at multiples of 8 rows of the frame (frame starts and
+  // spans are multiples of 16, stages of 8 rows): row j then always meets
+  // the lane of row class j % 8, whose chunk order it is reduced in, so a
+  // row's results do not depend on how many items the launch cuts.
   const int2 sp = span(a, it.g);
-  it.row0 = sp.x + (int)(((int64_t)sp.y * c) / a.chunks);
-  it.rows = sp.x + (int)(((int64_t)sp.y * (c + 1)) / a.chunks) - it.row0;
+  it.row0 = sp.x + (int)((((int64_t)sp.y * c) / it.C) & ~7LL);
+  it.rows = sp.x + (int)((((int64_t)sp.y * (c + 1)) / it.C) & ~7LL) - it.row0;
   it.hf = (int64_t)it.h * a.Nf + it.g;
-  it.pi = it.hf * a.chunks + c;
+  it.pi = it.hf * it.C + c;
   return it;
 }
 
@@ -344,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
   int chunk[NCH];
 #pragma unroll
   for (int j = 0; j < NCH; ++j) chunk[j] = sg + 4 * (j ^ xr);
-  const int H = a.H, Nf = a.Nf, C = a.chunks;
-  const int total = 3 * H * Nf * C;
+  const int H = a.H, Nf = a.Nf;
+  const int total = H * Nf * (a.chunks_k + 2 * a.chunks_q);
   unsigned* const queue = a.sync;
   unsigned* const keys_frame_done = a.sync + 1;  // [H, Nf] items done per frame and phase
   unsigned* const cent_frame_done = keys_frame_done + H * Nf;
@@ -499,11 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
             dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
           }
         }
-        if (warp_finish(&keys_frame_done[A.hf], C, lane)) {
+        if (warp_finish(&keys_frame_done[A.hf], A.C, lane)) {
           // The frame's key sums, in chunk order.
           constexpr int CPL = D / 32;
           float s[CPL];
-          ordered_sum<CPL>(a.ksum_part + A.hf * C * D + lane * CPL, C, D, s);
+          ordered_sum<CPL>(a.ksum_part + A.hf * A.C * D + lane * CPL, A.C, D, s);
 #pragma unroll
           for (int e = 0; e < CPL; ++e) a.fsum[A.hf * D + lane * CPL + e] = s[e];
           if (warp_finish(&keys_done[A.h], Nf, lane)) {
@@ -573,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
           break;
         best = warp_max(best);
         if (lane == 0) a.kmax_part[A.pi] = best;
-        if (warp_finish(&cent_frame_done[A.hf], C, lane)) {
-          const float mx = warp_max_of(a.kmax_part + A.hf * C, C, 0.f, lane);
+        if (warp_finish(&cent_frame_done[A.hf], A.C, lane)) {
+          const float mx = warp_max_of(a.kmax_part + A.hf * A.C, A.C, 0.f, lane);
           if (lane == 0) a.frame_max[A.hf] = sqrtf(mx);
           if (warp_finish(&cent_done[A.h], Nf, lane)) {
             // Per query frame: the largest maximum of the frames it sees.
@@ -634,8 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
           break;
         gmax = warp_max(gmax);
         if (lane == 0) a.gmax_part[A.pi] = gmax;
-        if (warp_finish(&qry_frame_done[A.hf], C, lane)) {
-          const float fm = warp_max_of(a.gmax_part + A.hf * C, C, -INFINITY, lane);
+        if (warp_finish(&qry_frame_done[A.hf], A.C, lane)) {
+          const float fm = warp_max_of(a.gmax_part + A.hf * A.C, A.C, -INFINITY, lane);
           if (lane == 0) a.gmax_frame[A.hf] = fm;
           if (warp_finish(&qry_done[A.h], Nf, lane)) {
             // Largest slack of the head (max is exact in any order).
@@ -702,7 +711,7 @@ int launch_d(const PrepassArgs& a, cudaStream_t st) {
   // gives up on a wait leaves every head on the safe path.
   if (cudaMemsetAsync(a.sync, 0, prepass_sync_words(a.H, a.Nf) * sizeof(unsigned), st) != cudaSuccess) return -1;
   if (cudaMemsetAsync(a.elig, 0, (size_t)a.H, st) != cudaSuccess) return -1;
-  const int items = 3 * a.H * a.Nf * a.chunks;
+  const int items = a.H * a.Nf * (a.chunks_k + 2 * a.chunks_q);
   const int grid = grid_size<D>(items);
   if (grid < 1) return -1;
   prepass_kernel<D><<<grid, kThreads, kSmemBytes, st>>>(a);
@@ -713,6 +722,16 @@ int launch_d(const PrepassArgs& a, cudaStream_t st) {
 }  // namespace
 
 size_t prepass_sync_words(int H, int Nf) { return 1 + 3 * (size_t)H * Nf + 6 * (size_t)H; }
+
+int prepass_chunks(int heads, int64_t rows_per_head, int span_max, int sms) {
+  // Items per phase: one per two warps.  More, smaller items measured
+  // slower (each item's reductions, counters and flag cost the same).
+  const int64_t target = (int64_t)(sms > 0 ? sms : 1) * kWarps / 2;
+  int64_t r = (int64_t)heads * rows_per_head / target / 8 * 8;
+  if (r < kPrepassMinRows) r = kPrepassMinRows;
+  if (r > kPrepassRows) r = kPrepassRows;
+  return (int)((span_max + r - 1) / r);
+}
 
 int launch_prepass(const PrepassArgs& a, cudaStream_t stream) {
   if (a.d == 128) return launch_d<128>(a, stream);

@@ -132,7 +132,7 @@ extern "C" int fas_prepass_noalloc(const void* q, const void* k, int frame_token
   a.Nf = (int)Nf;
   a.H = H;
   a.d = d;
-  a.chunks = chunks;
+  a.chunks_k = a.chunks_q = chunks;
   a.scale = (float)(1.0 / sqrt((double)d));
   a.limit_ns = kWaitLimitNs;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
