@@ -24,7 +24,7 @@ struct State {
   HostPlan plan;
   int device = -1;
   int sms = 0;            // SMs of the plan's device
-  int chunks_k = 0;       // prepass key items per frame (fixed per plan: the frame sums' order)
+  int chunks_k = 0;       // prepass key items per frame (set by the frame span: the frame sums' order)
   size_t part_items = 0;  // per-item slots of the prepass's centred and query partials (the largest launch)
   void* arena = nullptr;
   int4* work = nullptr;
@@ -145,11 +145,12 @@ int allocate(const HostPlan& p) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FAS_ERR_CUDA;
-  // The key items per frame follow the plan (so the frame sums, added in
-  // chunk order, are the same in every launch); a launch over nh heads
-  // holds nh * Nf * chunks(nh) centred and query partials, and the host
-  // pipeline launches over head groups of any size up to H.
-  s.chunks_k = fas::prepass_chunks(p.H, p.N, p.T, s.sms);
+  // Key items per frame depend on the frame span alone (so a head's frame
+  // sums, added in chunk order, are the same in every launch and in every
+  // plan, whatever its number of heads); a launch over nh heads holds
+  // nh * Nf * chunks(nh) centred and query partials, and the host pipeline
+  // launches over head groups of any size up to H.
+  s.chunks_k = (p.T + fas::kPrepassRows - 1) / fas::kPrepassRows;
   s.part_items = 0;
   for (int nh = 1; nh <= p.H; ++nh) {
     const size_t items = (size_t)nh * Nf * fas::prepass_chunks(nh, p.N, p.T, s.sms);

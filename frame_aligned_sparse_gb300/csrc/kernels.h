@@ -59,7 +59,7 @@ struct PrepassArgs {
   int64_t N;
   int T;                // frame span when spans is null; else the largest span
   int Nf, H, d;
-  int chunks_k;         // key items per frame (sets the frame sums' order: fixed per plan)
+  int chunks_k;         // key items per frame (sets the frame sums' order: fixed by the frame span)
   int chunks_q;         // centred and query items per frame (any count >= 1)
   float scale;          // 1/sqrt(d)
   uint64_t limit_ns;    // bound on each wait for another item's result
