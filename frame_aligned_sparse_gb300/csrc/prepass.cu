@@ -681,24 +681,19 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
   }
 }
 
-// Resident CTAs per SM of the kernel for one head dimension (looked up once
-// per process; every device of one process is assumed to be a GB300).
+// CTAs of a launch: the kernel's resident CTAs per SM on the current device
+// (its shared-memory opt-in is set on every call: the attribute belongs to
+// the device's context), at most one item per warp.
 template <int D>
 int grid_size(int items) {
-  static int per_sm = 0, sms = 0;
-  if (per_sm == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(prepass_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepass_kernel<D>, kThreads, kSmemBytes) !=
-            cudaSuccess ||
-        per_sm < 1) {
-      per_sm = 0;
-      return -1;
-    }
-  }
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaFuncSetAttribute(prepass_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepass_kernel<D>, kThreads, kSmemBytes) != cudaSuccess ||
+      per_sm < 1)
+    return -1;
   const int g = per_sm * sms;
   const int need = (items + kWarps - 1) / kWarps;  // one item per warp at least
   return g < need ? g : need;
