@@ -50,6 +50,15 @@ namespace {
 #define FAS_PROLOGUE_CLUSTER 2
 #endif
 constexpr int kClusterP = FAS_PROLOGUE_CLUSTER;  // CTAs that share each W' tile (TMA multicast)
+#ifndef FAS_PROLOGUE_KEEP_X
+#define FAS_PROLOGUE_KEEP_X 1
+#endif
+#ifndef FAS_PROLOGUE_KEEP_W
+#define FAS_PROLOGUE_KEEP_W 1
+#endif
+#ifndef FAS_PROLOGUE_STREAM_OUT
+#define FAS_PROLOGUE_STREAM_OUT 1
+#endif
 constexpr int kThreadsP = 192;
 constexpr int kStagesP = 4;
 constexpr int kKStep = 64;   // K elements per stage: one 128-byte swizzle row of bf16
@@ -142,7 +151,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       // first-tile fills, by this CTA's row sums).
       // x (each panel read once per column tile) and W' (read by every
       // panel of the part) stay in L2 ahead of the q, k, v stream.
-      const uint64_t keep = ptx::policy_evict_last();
+      const uint64_t keep_x = FAS_PROLOGUE_KEEP_X ? ptx::policy_evict_last() : ptx::policy_evict_normal();
+      const uint64_t keep_w = FAS_PROLOGUE_KEEP_W ? ptx::policy_evict_last() : ptx::policy_evict_normal();
       int fill = 0;
       bool ok = true;
       for (int n = 0; ok && n < ncol; ++n)
@@ -160,12 +170,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           const uint32_t dst = ring + s * kStageBytes;
           const uint32_t fb = ptx::smem_addr(&bars.full[s]);
           ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-          ptx::tma_load_2d_hint(dst, &tm_x, fb, kk * kKStep, panel * kRows, keep);
+          ptx::tma_load_2d_hint(dst, &tm_x, fb, kk * kKStep, panel * kRows, keep_x);
           if (CL == 1)
-            ptx::tma_load_2d_hint(dst + kABytes, &tm_w, fb, kk * kKStep, part * p.heads * D + n * TN, keep);
+            ptx::tma_load_2d_hint(dst + kABytes, &tm_w, fb, kk * kKStep, part * p.heads * D + n * TN, keep_w);
           else
             ptx::tma_load_2d_multicast_hint(dst + kABytes + rank * (kBBytes / CL), &tm_w, fb, kk * kKStep,
-                                            part * p.heads * D + n * TN + (int)rank * (TN / CL), kMask, keep);
+                                            part * p.heads * D + n * TN + (int)rank * (TN / CL), kMask, keep_w);
         }
       if (!ok) {
         // Let the copies already started land before the CTA exits (a
@@ -253,7 +263,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       ptx::mbar_arrive(ptx::smem_addr(&bars.rowsum[s]));
     }
     const float rstd = rsqrtf((ss0 + ss1) / (float)p.width + p.eps);
-    const uint64_t stream = ptx::policy_evict_first();  // q, k, v: written once here, read by later kernels
+    // q, k, v: written once here, read by later kernels.
+    const uint64_t stream = FAS_PROLOGUE_STREAM_OUT ? ptx::policy_evict_first() : ptx::policy_evict_normal();
     uint16_t* const out = static_cast<uint16_t*>(part == 0 ? p.q : part == 1 ? p.k : p.v);
     const float* const ctab = p.cos_tab + (valid ? token : 0) * (D / 2);
     const float* const stab = p.sin_tab + (valid ? token : 0) * (D / 2);
