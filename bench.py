@@ -86,6 +86,33 @@ def pinned_copy_gbs(host_in, host_out, dev_buf, stream):
     return res
 
 
+def copy_overlap_ms(pin, step):
+    """Wall ms of the step's host-to-device copies alone (pinned q, k, v into
+    scratch device buffers on a side stream), of one device step alone, and
+    of both at once: whether this box runs copies beside the kernels, which
+    sets how far the end-to-end figure can follow the device one."""
+    import time
+    import torch
+    scratch = {t: torch.empty(pin[t].shape, dtype=pin[t].dtype, device="cuda") for t in "qkv"}
+    side = torch.cuda.Stream()
+
+    def copies():
+        with torch.cuda.stream(side):
+            for t in "qkv":
+                scratch[t].copy_(pin[t], non_blocking=True)
+
+    res = {}
+    for name, fn in (("copies_ms", copies), ("compute_ms", step), ("both_ms", lambda: (step(), copies()))):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        fn()
+        torch.cuda.synchronize()
+        res[name] = (time.perf_counter() - t0) * 1e3
+    del scratch
+    return res
+
+
 def job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
     """Whole-job throughput: every rank runs its own chunk (replicas, weak
     scaling), so the job does world * steps chunks in the slowest rank's
@@ -413,6 +440,7 @@ def run_fas(args, w):
     h2d = sum(pin[t].numel() * 2 for t in "qkv")
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
     copy_gbs = pinned_copy_gbs(pin["q"], out_h, q, stream)
+    overlap = copy_overlap_ms(pin, step)
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
@@ -517,7 +545,8 @@ def run_fas(args, w):
                 # Copy bandwidth between these pinned buffers and the device,
                 # taken outside the timed region: the host side of the box
                 # sets how far the copies can hide behind the kernels.
-                "pinned_h2d_gbs": copy_gbs[0], "pinned_d2h_gbs": copy_gbs[1]},
+                "pinned_h2d_gbs": copy_gbs[0], "pinned_d2h_gbs": copy_gbs[1],
+                "overlap_check": overlap},
         "gpu_launches": timed_launches,
         "clocks": clocks,
         "ablation": abl,
