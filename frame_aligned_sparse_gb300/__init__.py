@@ -26,6 +26,7 @@ __all__ = [
     "fas_status", "fas_prepass_readback", "fas_selftest_wait_timeout", "fas_last_launch_count",
     "fas_prepass_noalloc", "fas_forward_host", "fas_set_layout", "LAYOUTS", "fas_forward_ablation",
     "fas_prologue", "fas_prologue_fold_weights", "PROLOGUE_LAYOUTS",
+    "fas_prologue_with_key_sums", "fas_prepass_with_key_sums", "key_sums_shape",
 ]
 
 FAS_OK, FAS_ERR_ARG, FAS_ERR_STATE, FAS_ERR_ALIGN, FAS_ERR_CUDA, FAS_ERR_TIMEOUT, FAS_ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
@@ -86,11 +87,14 @@ _SIGS = {
     "fas_plan_describe_ragged": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_int] * 6 +
                                  [ctypes.POINTER(_PlanInfoC), ctypes.c_void_p, ctypes.c_void_p]),
     "fas_prepass": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "fas_prepass_with_key_sums": (ctypes.c_int, [ctypes.c_void_p] * 5),
     "fas_forward": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_void_p]),
     "fas_forward_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "fas_forward_ablation": (ctypes.c_int, [ctypes.c_void_p] * 6),
     "fas_prologue": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 + [ctypes.c_float] +
                      [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]),
+    "fas_prologue_with_key_sums": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 + [ctypes.c_float] +
+                                   [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p] * 2),
     "fas_prologue_fold_weights": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p]),
     "fas_free": (ctypes.c_int, []),
     "fas_status": (ctypes.c_int, [ctypes.c_void_p]),
@@ -244,6 +248,29 @@ def fas_prepass(q, k, stream=None, want_elig: bool = False) -> Optional[np.ndarr
     return elig
 
 
+def key_sums_shape(heads: int, tokens: int, head_dim: int) -> tuple:
+    """Shape of the 16-token key column sums: [H, N/16, d] (fp32)."""
+    if tokens % 16:
+        raise ValueError(f"tokens ({tokens}) must be a multiple of 16 for key sums")
+    return (heads, tokens // 16, head_dim)
+
+
+def fas_prepass_with_key_sums(q, k, key_sums, stream=None, want_elig: bool = False) -> Optional[np.ndarray]:
+    """fas_prepass with the key column sums per 16 tokens given (fp32
+    [H, N/16, d], e.g. from fas_prologue_with_key_sums): k is read once."""
+    import torch
+    shape = _qkv_shape()
+    _check_tensor("q", q, shape, torch.bfloat16)
+    _check_tensor("k", k, shape, torch.bfloat16)
+    _check_tensor("key_sums", key_sums, key_sums_shape(_PLAN["heads"], _PLAN["tokens"], _PLAN["head_dim"]),
+                  torch.float32)
+    elig = np.zeros(_PLAN["heads"], dtype=np.uint8) if want_elig else None
+    rc = load().fas_prepass_with_key_sums(q.data_ptr(), k.data_ptr(), key_sums.data_ptr(), _stream_handle(stream),
+                                          elig.ctypes.data if want_elig else None)
+    _check("fas_prepass_with_key_sums", rc)
+    return elig
+
+
 def fas_forward(q, k, v, out=None, lse=None, mode: str = "auto", stream=None):
     """Attention; returns (out bf16 [H, N, d], lse fp32 [H, N])."""
     import torch
@@ -304,6 +331,21 @@ def fas_prologue(x, w_folded, cos, sin, heads: int, head_dim: int, layout: str =
     (see ``fas_prologue`` in fas.h).  x bf16 [N, C]; w_folded bf16
     [3*H*d, C]; cos, sin fp32 [N, d/2].  Returns (q, k, v) bf16 in
     ``layout``: "hnd" [H, N, d], "nhd" [N, H, d] or "a2a" [G, P, N, H/(G*P), d]."""
+    return _prologue(x, w_folded, cos, sin, heads, head_dim, layout, groups, ranks, q, k, v, False, None, eps,
+                     stream)
+
+
+def fas_prologue_with_key_sums(x, w_folded, cos, sin, heads: int, head_dim: int, layout: str = "hnd",
+                               groups: int = 1, ranks: int = 1, q=None, k=None, v=None, key_sums=None,
+                               eps: float = RMS_EPS, stream=None):
+    """fas_prologue that also writes the column sums of the written k over
+    each 16 tokens (fp32 [H, N/16, d], the input of
+    fas_prepass_with_key_sums).  Returns (q, k, v, key_sums)."""
+    return _prologue(x, w_folded, cos, sin, heads, head_dim, layout, groups, ranks, q, k, v, True, key_sums, eps,
+                     stream)
+
+
+def _prologue(x, w_folded, cos, sin, heads, head_dim, layout, groups, ranks, q, k, v, sums, key_sums, eps, stream):
     import torch
     N, C = x.shape
     _check_tensor("x", x, (N, C), torch.bfloat16)
@@ -326,11 +368,22 @@ def fas_prologue(x, w_folded, cos, sin, heads: int, head_dim: int, layout: str =
             t = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
         _check_tensor(name, t, shape, torch.bfloat16)
         outs.append(t)
-    rc = load().fas_prologue(x.data_ptr(), w_folded.data_ptr(), cos.data_ptr(), sin.data_ptr(), N, C, heads,
-                             head_dim, float(eps), outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
-                             PROLOGUE_LAYOUTS[layout], groups, ranks, _stream_handle(stream))
-    _check("fas_prologue", rc)
-    return tuple(outs)
+    if not sums:
+        rc = load().fas_prologue(x.data_ptr(), w_folded.data_ptr(), cos.data_ptr(), sin.data_ptr(), N, C, heads,
+                                 head_dim, float(eps), outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
+                                 PROLOGUE_LAYOUTS[layout], groups, ranks, _stream_handle(stream))
+        _check("fas_prologue", rc)
+        return tuple(outs)
+    ks_shape = key_sums_shape(heads, N, head_dim)
+    if key_sums is None:
+        key_sums = torch.empty(ks_shape, dtype=torch.float32, device=x.device)
+    _check_tensor("key_sums", key_sums, ks_shape, torch.float32)
+    rc = load().fas_prologue_with_key_sums(x.data_ptr(), w_folded.data_ptr(), cos.data_ptr(), sin.data_ptr(), N, C,
+                                           heads, head_dim, float(eps), outs[0].data_ptr(), outs[1].data_ptr(),
+                                           outs[2].data_ptr(), PROLOGUE_LAYOUTS[layout], groups, ranks,
+                                           key_sums.data_ptr(), _stream_handle(stream))
+    _check("fas_prologue_with_key_sums", rc)
+    return (*outs, key_sums)
 
 
 def _check_host_tensor(name, t, shape, dtype):

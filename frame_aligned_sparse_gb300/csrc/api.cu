@@ -237,6 +237,7 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   a.fvis = s.fvis;
   a.R0 = p.R0;
   a.r = p.r;
+  a.key_sums = nullptr;
   a.ksum_part = s.ksum_part;  // launches run one at a time (one stream)
   a.kmax_part = s.kmax_part;
   a.gmax_part = s.gmax_part;
@@ -564,16 +565,19 @@ int fas_plan_ragged(const int32_t* frame_tokens, int n_frames, int ref_frames, i
   return make_plan(frame_tokens, 0, n_frames, ref_frames, window_radius, heads, head_dim, block_k, info);
 }
 
-int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_host) {
+namespace {
+
+int run_prepass(const void* q, const void* k, const float* key_sums, void* cuda_stream, uint8_t* elig_host) {
   if (!g_state.planned) return FAS_ERR_STATE;
   if (!q || !k) return FAS_ERR_ARG;
-  if (!aligned16(q) || !aligned16(k)) return FAS_ERR_ALIGN;
+  if (!aligned16(q) || !aligned16(k) || (key_sums && !aligned16(key_sums))) return FAS_ERR_ALIGN;
   int rc = check_device();
   if (rc != FAS_OK) return rc;
   const HostPlan& p = g_state.plan;
   State& s = g_state;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  const fas::PrepassArgs a = prepass_args(q, k, 0, p.H);
+  fas::PrepassArgs a = prepass_args(q, k, 0, p.H);
+  a.key_sums = key_sums;
   const int n = fas::launch_prepass(a, st);
   s.last_launches = n > 0 ? n : 0;
   if (n < 0) return FAS_ERR_CUDA;
@@ -587,6 +591,18 @@ int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_h
     if (cudaMemcpy(elig_host, s.elig, (size_t)p.H, cudaMemcpyDeviceToHost) != cudaSuccess) return FAS_ERR_CUDA;
   }
   return FAS_OK;
+}
+
+}  // namespace
+
+int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_host) {
+  return run_prepass(q, k, nullptr, cuda_stream, elig_host);
+}
+
+int fas_prepass_with_key_sums(const void* q, const void* k, const float* key_sums, void* cuda_stream,
+                              uint8_t* elig_host) {
+  if (!key_sums) return FAS_ERR_ARG;
+  return run_prepass(q, k, key_sums, cuda_stream, elig_host);
 }
 
 int fas_forward(const void* q, const void* k, const void* v, void* out, float* lse, int mode, void* cuda_stream) {
@@ -745,7 +761,16 @@ int fas_forward_ablation(const void* q, const void* k, const void* v, void* out,
 int fas_prologue(const void* x, const void* w_folded, const float* cos_tab, const float* sin_tab, int tokens,
                  int width, int heads, int head_dim, float eps, void* q, void* k, void* v, int layout, int groups,
                  int ranks, void* cuda_stream) {
+  return fas_prologue_with_key_sums(x, w_folded, cos_tab, sin_tab, tokens, width, heads, head_dim, eps, q, k, v,
+                                    layout, groups, ranks, nullptr, cuda_stream);
+}
+
+int fas_prologue_with_key_sums(const void* x, const void* w_folded, const float* cos_tab, const float* sin_tab,
+                               int tokens, int width, int heads, int head_dim, float eps, void* q, void* k, void* v,
+                               int layout, int groups, int ranks, float* key_sums, void* cuda_stream) {
   if (!x || !w_folded || !cos_tab || !sin_tab || !q || !k || !v) return FAS_ERR_ARG;
+  if (key_sums && tokens % 16 != 0) return FAS_ERR_ARG;
+  if (key_sums && !aligned16(key_sums)) return FAS_ERR_ALIGN;
   if (tokens < 1 || width < 64 || width % 64 != 0 || (head_dim != 64 && head_dim != 128) || heads < 1 ||
       fas::prologue_tile_cols(heads, head_dim) == 0 || !(eps >= 0.f))
     return FAS_ERR_ARG;
@@ -781,6 +806,7 @@ int fas_prologue(const void* x, const void* w_folded, const float* cos_tab, cons
   pp.layout = layout;
   pp.groups = layout == FAS_LAYOUT_A2A ? groups : 1;
   pp.ranks = layout == FAS_LAYOUT_A2A ? ranks : 1;
+  pp.key_sums = key_sums;
   pp.eps = eps;
   pp.err = err;
   pp.limit_ns = fas::kWaitLimitNs;

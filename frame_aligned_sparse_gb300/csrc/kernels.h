@@ -42,6 +42,7 @@ struct PrepassArgs {
   const int2* spans;    // [Nf] {first token, tokens} of each frame; null: frame g is [g*T, (g+1)*T)
   const int4* fvis;     // [Nf] frames visible from f: [x, y) and [z, w); null: the frame rule with R0, r
   int R0, r;            // reference frames and window radius (used when fvis is null)
+  const float* key_sums = nullptr;  // null (the key items read k), or [H, N / 16, d] key sums per 16 rows
   float* ksum_part;     // [H, Nf, chunks_k, d] per-item key column sums
   float* kmax_part;     // [H, Nf, chunks_q]    per-item max |k - mu|^2
   float* gmax_part;     // [H, Nf, chunks_q]    per-item max slack
@@ -136,6 +137,8 @@ struct PrologueParams {
   int heads, head_dim;    // H, d; H * d a multiple of 128
   int layout;             // FAS_LAYOUT_HND, FAS_LAYOUT_NHD or FAS_LAYOUT_A2A
   int groups, ranks;      // the all-to-all layout's G and P
+  float* key_sums = nullptr;  // null, or fp32 [heads, tokens / 16, head_dim]: column sums of the
+                              // written k over each group of 16 tokens (tokens a multiple of 16)
   float eps;
   unsigned int* err;      // device error word
   uint64_t limit_ns;

@@ -15,8 +15,11 @@
 // G_i bounds the gap between b_i and the true centred row maximum.
 //
 // One persistent kernel, one CTA of sixteen warps per SM, in which every warp
-// works on its own.  A work item is (phase, head, frame, chunk of at most
-// 256 of the frame's rows) and belongs to one warp.  The warp streams the
+// works on its own.  A work item is (phase, head, frame, chunk of the frame's
+// rows) and belongs to one warp.  Key chunks are fixed by the frame span
+// (about 256 rows), which fixes the order the frame's key sums are added in;
+// centred and query chunks are sized (32 to 256 rows) for about one item per
+// two warps of the grid in each phase.  The warp streams the
 // rows through a private ring of shared-memory stages that bulk copies
 // (cp.async.bulk, completing on an mbarrier) fill ahead of it, running into
 // the next item's rows (input data, ready whatever the next item waits for)
@@ -45,9 +48,8 @@
 // A stage (6 KB; two per warp) holds up to 24 rows (d = 128) or 48 rows
 // (d = 64): one bulk copy when a head's rows are contiguous (the head-major
 // [H, N, d] layout), one per row otherwise (token-major [N, H, d], rows H*d
-// elements apart).  Each phase keeps only its own registers (126 at most),
-// so sixteen warps fit on an SM.  Four
-// lanes share a row, each with a fixed quarter of the columns (and the
+// elements apart).  Each phase keeps only its own registers (128 at most at
+// d = 128), so sixteen warps fit on an SM.  Four lanes share a row, each with a fixed quarter of the columns (and the
 // matching quarter of mu_h and kbar_c in registers), so a row's dot
 // products and norms need two shuffle steps and the key sums none until
 // the item ends; the arithmetic runs on packed fp32 pairs (fma.rn.f32x2,
@@ -248,10 +250,12 @@ __device__ __forceinline__ Item decode(const PrepassArgs& a, int item) {
   // Chunk boundaries at multiples of 8 rows of the frame (frame starts and
   // spans are multiples of 16, stages of 8 rows): row j then always meets
   // the lane of row class j % 8, whose chunk order it is reduced in, so a
-  // row's results do not depend on how many items the launch cuts.
+  // row's results do not depend on how many items the launch cuts.  Key
+  // items that read given 16-row key sums cut at multiples of 16.
+  const int64_t cut = it.phase == kKeys && a.key_sums ? ~15LL : ~7LL;
   const int2 sp = span(a, it.g);
-  it.row0 = sp.x + (int)((((int64_t)sp.y * c) / it.C) & ~7LL);
-  it.rows = sp.x + (int)((((int64_t)sp.y * (c + 1)) / it.C) & ~7LL) - it.row0;
+  it.row0 = sp.x + (int)((((int64_t)sp.y * c) / it.C) & cut);
+  it.rows = sp.x + (int)((((int64_t)sp.y * (c + 1)) / it.C) & cut) - it.row0;
   it.hf = (int64_t)it.h * a.Nf + it.g;
   it.pi = it.hf * it.C + c;
   return it;
@@ -315,7 +319,11 @@ struct Ring {
   __device__ __forceinline__ uint32_t stage_buf(unsigned n) const { return buf + (n % kStages) * kStageBytes; }
   __device__ __forceinline__ uint32_t stage_bar(unsigned n) const { return bar + (n % kStages) * 8; }
 
-  static __device__ __forceinline__ int stages(const Item& it) { return (it.rows + kRowsPerStage - 1) / kRowsPerStage; }
+  // Stages of the item's rows (none for key items given 16-row key sums).
+  static __device__ __forceinline__ int stages(const PrepassArgs& a, const Item& it) {
+    if (it.phase == kKeys && a.key_sums) return 0;
+    return (it.rows + kRowsPerStage - 1) / kRowsPerStage;
+  }
 
   // Copies stage t of the item (its rows t*kRowsPerStage ..) into the next
   // slot.  Warp-wide.
@@ -386,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
   const int ia = (int)__shfl_sync(0xffffffffu, raw, 0);
   if (ia < total) {
     Item A = decode(a, ia), B = A;
-    int nA = R::stages(A), tA = 0, nB = 0, tB = 0;
+    int nA = R::stages(a, A), tA = 0, nB = 0, tB = 0;
     unsigned rawB = 0;
     if (lane == 0) rawB = atomicAdd(queue, 1u);
     int ib = -1;        // B's index, once looked at
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
         if (ib >= total) break;
         if (!hasB) {
           B = decode(a, ib);
-          nB = R::stages(B);
+          nB = R::stages(a, B);
           tB = 0;
           hasB = true;
         }
@@ -451,7 +459,37 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
         }
       };
 
-      if (A.phase == kKeys) {
+      if (A.phase == kKeys && a.key_sums) {
+        // Column sums of the chunk's keys from its 16-row group sums, added
+        // in group order; lane l owns columns CPL l .. CPL l + CPL - 1.
+        constexpr int CPL = D / 32;
+        constexpr int U = 8;  // groups loaded ahead of their additions
+        const float* src = a.key_sums + ((int64_t)A.h * (a.N / 16) + A.row0 / 16) * D + lane * CPL;
+        const int ng = A.rows / 16;
+        float s[CPL];
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) s[e] = 0.f;
+        for (int g0 = 0; g0 < ng; g0 += U) {
+          float v[U][CPL];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            if (g0 + u < ng) {
+              load_cols<CPL>(src + (int64_t)(g0 + u) * D, v[u]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < CPL; ++e) v[u][e] = 0.f;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (g0 + u < ng) {
+#pragma unroll
+              for (int e = 0; e < CPL; ++e) s[e] += v[u][e];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) a.ksum_part[A.pi * D + lane * CPL + e] = s[e];
+      } else if (A.phase == kKeys) {
         // Column sums of the chunk's keys.
         uint64_t acc2[NCH][4];
 #pragma unroll
@@ -508,6 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
             dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
           }
         }
+      }
+      if (A.phase == kKeys) {
         if (warp_finish(&keys_frame_done[A.hf], A.C, lane)) {
           // The frame's key sums, in chunk order.
           constexpr int CPL = D / 32;
@@ -662,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepass_kernel(const PrepassArgs 
       if (ib >= total) break;
       if (!hasB) {
         B = decode(a, ib);
-        nB = R::stages(B);
+        nB = R::stages(a, B);
         tB = 0;
       }
       A = B;

@@ -113,6 +113,7 @@ extern "C" int fas_prepass_noalloc(const void* q, const void* k, int frame_token
   a.fvis = nullptr;                 // visible frames from the frame rule
   a.R0 = R0;
   a.r = r;
+  a.key_sums = nullptr;             // the key items read k
   a.ksum_part = static_cast<float*>(part[0]);
   a.kmax_part = static_cast<float*>(part[1]);
   a.gmax_part = static_cast<float*>(part[2]);

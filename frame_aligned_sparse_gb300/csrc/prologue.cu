@@ -32,6 +32,15 @@
 //              only permutes 16-byte pieces inside a row); then per tile the
 //              epilogue: TMEM -> registers, times 1/rms, rotary (q, k),
 //              round to bf16, stores in the output layout.
+//
+// Optionally the k part also writes, per head, the column sums of the
+// rounded keys over each group of 16 tokens, the statistic the prepass's
+// key phase would otherwise compute by reading k back ("Unchaining the
+// Softmax": the mean key and the per-frame key sums).  Frames start at
+// multiples of 16 tokens, so no group crosses a frame.  A group is the 16
+// rows of a half-warp; its column sums are reduced by recursive halving
+// across the half-warp (four exchange steps, 30 shuffles per 32 columns),
+// after which each lane holds two columns' sums.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -77,6 +86,21 @@ struct PBars {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Recursive halving across the lanes of a half-warp: on entry v[0 .. W) are
+// this lane's W columns; afterwards v[0 .. W/2) are column sums over lanes
+// l and l ^ O of the half that this lane keeps (the upper half of the
+// columns when bit O of its lane index is set).
+template <int W, int O>
+__device__ __forceinline__ void halve(float (&v)[32], int lane) {
+  const bool up = (lane & O) != 0;
+#pragma unroll
+  for (int i = 0; i < W / 2; ++i) {
+    const float send = up ? v[i] : v[i + W / 2];
+    const float keep = up ? v[i + W / 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+  }
+}
 
 // Element offset of (head h, token n) in the output layout.
 __device__ __forceinline__ int64_t out_offset(const PrologueParams& p, int h, int64_t n) {
@@ -266,6 +290,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // q, k, v: written once here, read by later kernels.
     const uint64_t stream = FAS_PROLOGUE_STREAM_OUT ? ptx::policy_evict_first() : ptx::policy_evict_normal();
     uint16_t* const out = static_cast<uint16_t*>(part == 0 ? p.q : part == 1 ? p.k : p.v);
+    // Key sums: this half-warp's group of 16 tokens.
+    const bool sums = part == 1 && p.key_sums != nullptr;
+    const int64_t groups16 = p.tokens / 16;
+    const int64_t grp = ((int64_t)panel * kRows + (warp % 4) * 32 + (lane & 16)) / 16;
     const float* const ctab = p.cos_tab + (valid ? token : 0) * (D / 2);
     const float* const stab = p.sin_tab + (valid ? token : 0) * (D / 2);
     for (int n = 0; ok && n < ncol; ++n) {
@@ -311,19 +339,43 @@ __global__ void __launch_bounds__(kThreadsP, 1)
               hi[e] = fmaf(x0, sn[e], x1 * cs[e]);
             }
           }
-          if (valid) {
-            uint32_t pl[8], ph[8];
+          uint32_t pl[8], ph[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              pl[e] = ptx::pack_bf16x2(lo[2 * e], lo[2 * e + 1]);
-              ph[e] = ptx::pack_bf16x2(hi[2 * e], hi[2 * e + 1]);
-            }
+          for (int e = 0; e < 8; ++e) {
+            pl[e] = ptx::pack_bf16x2(lo[2 * e], lo[2 * e + 1]);
+            ph[e] = ptx::pack_bf16x2(hi[2 * e], hi[2 * e + 1]);
+          }
+          if (valid) {
             uint4* d0 = reinterpret_cast<uint4*>(dst + c * 16);
             uint4* d1 = reinterpret_cast<uint4*>(dst + D / 2 + c * 16);
             ptx::st_global_hint(d0, make_uint4(pl[0], pl[1], pl[2], pl[3]), stream);
             ptx::st_global_hint(d0 + 1, make_uint4(pl[4], pl[5], pl[6], pl[7]), stream);
             ptx::st_global_hint(d1, make_uint4(ph[0], ph[1], ph[2], ph[3]), stream);
             ptx::st_global_hint(d1 + 1, make_uint4(ph[4], ph[5], ph[6], ph[7]), stream);
+          }
+          if (sums) {
+            // The 16 rows of this half-warp, columns 16c .. 16c+15 (v[0 .. 16))
+            // and d/2 + 16c .. (v[16 .. 32)), as rounded and stored; rows
+            // past the last token count as zero.
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              v[2 * e] = valid ? bf16_lo(pl[e]) : 0.f;
+              v[2 * e + 1] = valid ? bf16_hi(pl[e]) : 0.f;
+              v[16 + 2 * e] = valid ? bf16_lo(ph[e]) : 0.f;
+              v[16 + 2 * e + 1] = valid ? bf16_hi(ph[e]) : 0.f;
+            }
+            halve<32, 8>(v, lane);
+            halve<16, 4>(v, lane);
+            halve<8, 2>(v, lane);
+            halve<4, 1>(v, lane);
+            // Lane l of the half holds columns 2 (l % 16) and 2 (l % 16) + 1
+            // of the 32.
+            const int li = lane & 15;
+            const int col = (li < 8 ? 0 : D / 2) + c * 16 + 2 * (li & 7);
+            if (grp < groups16)
+              *reinterpret_cast<float2*>(p.key_sums + ((int64_t)head * groups16 + grp) * D + col) =
+                  make_float2(v[0], v[1]);
           }
         }
       }

@@ -146,11 +146,11 @@ int fas_plan_describe_ragged(const int32_t* frame_tokens, int n_frames, int ref_
                              int32_t* work);
 
 /* Prepass ("Unchaining the Softmax": precomputed norms, mean-centred keys).
- * Reads q and k (device, bf16, in the current layout: [H, N, d] by
- * default) once each from device memory (one kernel; the second pass over a
- * head's keys is served from L2) and computes per head the mean key mu_h,
- * per key frame the
- * largest centred key norm, and per row
+ * Reads q (device, bf16, in the current layout: [H, N, d] by default) once
+ * and k twice (one kernel: the key sums, then, once mu_h is known, the
+ * centred norms; fas_prepass_with_key_sums skips the first read) and
+ * computes per head the mean key mu_h, per key frame the largest centred
+ * key norm, and per row
  *   m_i = s q_i.mu_h + s |q_i| max_{visible frames g} max_{j in g} |k_j - mu_h|
  * (an upper bound on the row's largest scaled logit), plus the eligibility
  * statistic stat_h = max_i (b_i - s q_i.kbar_c(i)) where b_i is the centred
@@ -161,6 +161,22 @@ int fas_plan_describe_ragged(const int32_t* frame_tokens, int n_frames, int ref_
  * bounded device wait gives up leaves every head ineligible (the online
  * path, correct for any input) and sets the device error word. */
 int fas_prepass(const void* q, const void* k, void* cuda_stream, uint8_t* elig_host);
+
+/* fas_prepass with the key column sums given instead of read from k: the
+ * kernel's key phase adds key_sums' groups instead of reading k, so k is
+ * read once (for the centred norms) and q once.  key_sums: device fp32
+ * [H, N/16, d], head-major whatever the layout of q and k, row (h, t) the
+ * column sums of head h's keys t*16 .. t*16 + 15, 16-byte aligned; written
+ * by fas_prologue_with_key_sums for the k it writes, or by the caller.
+ * Frames start at multiples of 16 tokens, so no group spans two frames.
+ * The frame sums and mu_h add the groups in a fixed order (results are
+ * bit-reproducible) that is not fas_prepass's, so the two calls' statistics
+ * agree to fp32 rounding, not bit for bit.  Sums that are not those of k
+ * give wrong bounds, which the attention's range guard (FAS_ERR_BOUND)
+ * catches only when they are far off.  Null key_sums: FAS_ERR_ARG;
+ * otherwise as fas_prepass (same plan, same q/k freshness rule). */
+int fas_prepass_with_key_sums(const void* q, const void* k, const float* key_sums, void* cuda_stream,
+                              uint8_t* elig_host);
 
 /* Attention.  q, k, v, out: device bf16 in the current layout ([H, N, d],
  * or [N, H, d] after fas_set_layout); lse: device fp32 [H, N].  Modes AUTO
@@ -332,6 +348,19 @@ int fas_prepass_noalloc(const void* q, const void* k, int frame_tokens, int n_fr
 int fas_prologue(const void* x, const void* w_folded, const float* cos_tab, const float* sin_tab, int tokens,
                  int width, int heads, int head_dim, float eps, void* q, void* k, void* v, int layout, int groups,
                  int ranks, void* cuda_stream);
+
+/* fas_prologue that also writes the prepass's key statistic, so that
+ * fas_prepass_with_key_sums need not read k back for it ("Layout Is the
+ * ABI": the producer writes what its consumer reads).  key_sums: device
+ * fp32 [heads, tokens/16, head_dim], 16-byte aligned (null: as
+ * fas_prologue); row (h, t) receives the column sums of head h's keys for
+ * tokens t*16 .. t*16 + 15 exactly as written to k (bf16 values added in
+ * fp32, in a fixed order).  In the all-to-all layout the tokens are the
+ * rank's own.  tokens must be a multiple of 16 (FAS_ERR_ARG); misaligned
+ * key_sums: FAS_ERR_ALIGN. */
+int fas_prologue_with_key_sums(const void* x, const void* w_folded, const float* cos_tab, const float* sin_tab,
+                               int tokens, int width, int heads, int head_dim, float eps, void* q, void* k, void* v,
+                               int layout, int groups, int ranks, float* key_sums, void* cuda_stream);
 
 /* Folds the RMSNorm scale into the projection weight once, for
  * fas_prologue: w_folded[o, c] = bf16(w[o, c] * gamma[c]) (nearest even).

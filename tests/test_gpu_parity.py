@@ -157,6 +157,81 @@ def test_prepass_statistics_720p():
     assert np.array_equal(elig.astype(bool), st["elig"])
 
 
+def key_sums_of(k_bits):
+    """Column sums of every 16 keys of each head, [H, N/16, d] fp32 on the
+    device, from the seeded bf16 keys [H, N, d] (fp64 sums rounded once):
+    the input fas_prepass_with_key_sums takes."""
+    H, N, d = k_bits.shape
+    out = np.empty((H, N // 16, d), np.float32)
+    for h in range(H):
+        out[h] = ref.bf16_bits_to_f64(k_bits[h]).reshape(N // 16, 16, d).sum(axis=1)
+    return torch.from_numpy(out).cuda()
+
+
+def check_key_sums_statistics(c, got, elig, row_atol=1e-3, rows=None):
+    st = c.stats
+    np.testing.assert_allclose(got["mu"], st["mu"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["frame_max"], st["M"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["stat"], st["stat"], rtol=1e-4, atol=1e-3)
+    sel = slice(None) if rows is None else rows
+    np.testing.assert_allclose(got["row_bound"][:, sel], st["m"][:, sel], rtol=1e-4, atol=row_atol)
+    assert np.array_equal(elig.astype(bool), st["elig"])
+    assert np.array_equal(got["elig"].astype(bool), st["elig"])
+
+
+def test_prepass_with_key_sums_720p():
+    """The prepass fed the 16-token key sums (its key phase adds them
+    instead of reading k) on the full 720p SR chunk, against the oracle."""
+    c = case("720p")
+    c.plan()
+    elig = fas.fas_prepass_with_key_sums(c.q, c.k, key_sums_of(c.x["k"]), want_elig=True)
+    got = fas.fas_prepass_readback(row_bound=True)
+    check_key_sums_statistics(c, got, elig, row_atol=2e-3, rows=c.rows)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_prepass_with_key_sums(name):
+    """Statistics against the oracle; against fas_prepass's to fp32
+    rounding (the sums are added in another order); bit-reproducible; the
+    attention on its bounds against the oracle."""
+    c = case(name)
+    c.plan()
+    ks = key_sums_of(c.x["k"])
+    runs = []
+    for _ in range(2):
+        elig = fas.fas_prepass_with_key_sums(c.q, c.k, ks, want_elig=True)
+        runs.append(fas.fas_prepass_readback(row_bound=True))
+    check_key_sums_statistics(c, runs[0], elig)
+    for key in runs[0]:
+        assert np.array_equal(runs[0][key], runs[1][key]), key
+    for mode in ("auto", "bounded"):
+        out, lse = fas.fas_forward(c.q, c.k, c.v, mode=mode)
+        assert fas.fas_status() == fas.FAS_OK
+        c.check(out, lse, f"{name}/{mode}/key sums")
+    fas.fas_prepass(c.q, c.k)
+    plain = fas.fas_prepass_readback(row_bound=True)
+    np.testing.assert_allclose(runs[0]["mu"], plain["mu"], rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(runs[0]["frame_max"], plain["frame_max"], rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(runs[0]["row_bound"], plain["row_bound"], rtol=1e-5, atol=1e-4)
+    assert np.array_equal(runs[0]["elig"], plain["elig"])
+
+
+def test_prepass_with_key_sums_errors():
+    c = case("tiny")
+    c.plan()
+    lib = fas.load()
+    ks = key_sums_of(c.x["k"])
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.fas_prepass_with_key_sums(c.q.data_ptr(), c.k.data_ptr(), None, st, None) == fas.FAS_ERR_ARG
+    assert lib.fas_prepass_with_key_sums(c.q.data_ptr(), c.k.data_ptr(), ks.data_ptr() + 4, st,
+                                         None) == fas.FAS_ERR_ALIGN
+    with pytest.raises((ValueError, TypeError)):
+        fas.fas_prepass_with_key_sums(c.q, c.k, ks[:, 1:])
+    fas.fas_free()
+    assert lib.fas_prepass_with_key_sums(c.q.data_ptr(), c.k.data_ptr(), ks.data_ptr(), st,
+                                         None) == fas.FAS_ERR_STATE
+
+
 def test_prepass_is_bit_reproducible():
     """Whichever CTA finishes a phase reduces in a fixed order: two runs give
     the same bits."""
@@ -476,6 +551,28 @@ def test_ragged_frames_full_rows(spec):
         assert np.abs(o - want["out"]).max() <= OUT_TOL, (name, mode)
         assert np.abs(l - want["lse"]).max() <= LSE_TOL, (name, mode)
     fas.fas_free()
+
+
+def test_ragged_frames_key_sums_token_major():
+    """The prepass fed the key sums on ragged frames (its key items cut at
+    16-token boundaries of every frame) with q, k token-major."""
+    name, H, d, R0, spans, r, sigma, seed = RAGGED[1]
+    F = len(spans) - R0
+    x = ragged_inputs(H, d, spans, sigma, seed)
+    st = ref.bound_statistics(x["q"], x["k"], spans, R0, r)
+    fas.fas_plan(spans, F, R0, r, H, d)
+    fas.fas_set_layout("nhd")
+    try:
+        q, k = (to_dev(to_nhd(x[t])) for t in "qk")
+        elig = fas.fas_prepass_with_key_sums(q, k, key_sums_of(x["k"]), want_elig=True)
+        got = fas.fas_prepass_readback(row_bound=True)
+    finally:
+        fas.fas_set_layout("hnd")
+        fas.fas_free()
+    assert np.array_equal(elig.astype(bool), st["elig"])
+    np.testing.assert_allclose(got["mu"], st["mu"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["frame_max"], st["M"], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(got["row_bound"], st["m"], rtol=1e-4, atol=1e-3)
 
 
 def test_ragged_frames_token_major_and_host_path():
