@@ -645,13 +645,16 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
     if (cudaStreamWaitEvent(st, s.ev_entry, 0) != cudaSuccess) return FAS_ERR_CUDA;
     if (s.exit_recorded && cudaStreamWaitEvent(st, s.ev_exit, 0) != cudaSuccess) return FAS_ERR_CUDA;
   }
-  // Work is submitted stream by stream (all copies in, then all compute,
-  // then all copies out): a copy-out that waits for its group's compute
-  // must never sit ahead of a later group's copy-in in a hardware queue the
-  // two directions might share.
-  for (int g = 0; g < groups; ++g) {
-    // In: the group's heads, one contiguous slice in [H, N, d]; in [N, H, d]
-    // a slice of every token's row, copied as a 2D block.
+  // Work is submitted breadth first: group g+1's copy in, group g's
+  // compute, group g-1's copy out.  Streams may share a hardware queue
+  // (the driver maps them onto a few connections), and a shared queue
+  // holds back whatever sits behind a command that waits.  In this order a
+  // waiting command only ever waits for work that is due before what
+  // follows it: a copy never sits behind compute it does not need, and
+  // compute never behind the copies of later groups.
+  auto copy_in = [&](int g) -> bool {
+    // The group's heads, one contiguous slice in [H, N, d]; in [N, H, d] a
+    // slice of every token's row, copied as a 2D block.
     const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
     const size_t off = (size_t)h0 * (size_t)head_stride();
     const void* src[3] = {q, k, v};
@@ -659,33 +662,39 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
     for (int t = 0; t < 3; ++t)
       if (copy_heads(dst[t] + off, static_cast<const uint16_t*>(src[t]) + off, nh, cudaMemcpyHostToDevice,
                      s.st_h2d) != cudaSuccess)
-        return FAS_ERR_CUDA;
-    if (cudaEventRecord(s.ev_in[g], s.st_h2d) != cudaSuccess) return FAS_ERR_CUDA;
-  }
-  for (int g = 0; g < groups; ++g) {
-    // Compute: prepass and attention for the group's heads.
+        return false;
+    return cudaEventRecord(s.ev_in[g], s.st_h2d) == cudaSuccess;
+  };
+  auto compute = [&](int g) -> bool {
+    // Prepass and attention for the group's heads.
     const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
-    if (cudaStreamWaitEvent(s.st_comp, s.ev_in[g], 0) != cudaSuccess) return FAS_ERR_CUDA;
+    if (cudaStreamWaitEvent(s.st_comp, s.ev_in[g], 0) != cudaSuccess) return false;
     const int np = fas::launch_prepass(prepass_args(s.dq, s.dk, h0, nh), s.st_comp);
-    if (np < 0) return FAS_ERR_CUDA;
+    if (np < 0) return false;
     launches += np;
     const int i0 = s.gwork_off[g], ni = s.gwork_off[g + 1] - i0;
     if (launch_fwd(s.io_tq, s.io_tk, s.io_tv, s.gwork + i0, ni, s.dout, s.dlse, mode, s.st_comp) != cudaSuccess)
-      return FAS_ERR_CUDA;
+      return false;
     ++launches;
-    if (cudaEventRecord(s.ev_done[g], s.st_comp) != cudaSuccess) return FAS_ERR_CUDA;
-  }
-  for (int g = 0; g < groups; ++g) {
-    // Out: the group's rows of out and lse.
+    return cudaEventRecord(s.ev_done[g], s.st_comp) == cudaSuccess;
+  };
+  auto copy_out = [&](int g) -> bool {
+    // The group's rows of out and lse.
     const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
     const size_t off = (size_t)h0 * (size_t)head_stride();
-    if (cudaStreamWaitEvent(s.st_d2h, s.ev_done[g], 0) != cudaSuccess) return FAS_ERR_CUDA;
-    if (copy_heads(static_cast<uint16_t*>(out) + off, s.dout + off, nh, cudaMemcpyDeviceToHost, s.st_d2h) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(lse + (size_t)h0 * p.N, s.dlse + (size_t)h0 * p.N, (size_t)nh * p.N * 4,
-                        cudaMemcpyDeviceToHost, s.st_d2h) != cudaSuccess)
-      return FAS_ERR_CUDA;
+    return cudaStreamWaitEvent(s.st_d2h, s.ev_done[g], 0) == cudaSuccess &&
+           copy_heads(static_cast<uint16_t*>(out) + off, s.dout + off, nh, cudaMemcpyDeviceToHost, s.st_d2h) ==
+               cudaSuccess &&
+           cudaMemcpyAsync(lse + (size_t)h0 * p.N, s.dlse + (size_t)h0 * p.N, (size_t)nh * p.N * 4,
+                           cudaMemcpyDeviceToHost, s.st_d2h) == cudaSuccess;
+  };
+  if (!copy_in(0)) return FAS_ERR_CUDA;
+  for (int g = 0; g < groups; ++g) {
+    if (g + 1 < groups && !copy_in(g + 1)) return FAS_ERR_CUDA;
+    if (!compute(g)) return FAS_ERR_CUDA;
+    if (g >= 1 && !copy_out(g - 1)) return FAS_ERR_CUDA;
   }
+  if (!copy_out(groups - 1)) return FAS_ERR_CUDA;
   // The caller's stream continues once every group's results are on the host.
   if (cudaEventRecord(s.ev_exit, s.st_d2h) != cudaSuccess) return FAS_ERR_CUDA;
   s.exit_recorded = true;
