@@ -449,15 +449,20 @@ def run_fas(args, w):
     for _ in range(3):  # first use builds the host pipeline and touches the pinned buffers
         e2e_step()
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    copy_before = pinned_copy_gbs(pin["q"], out_h, q, stream)
+    # One event after each call (the caller's stream resumes when the call's
+    # results are on the host): the spread of the per-call times shows
+    # whether the copies kept pace throughout.
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
     if world > 1:
         dist.barrier()
-    e0.record(stream)
-    for _ in range(e2e_steps):
+    ev[0].record(stream)
+    for i in range(e2e_steps):
         e2e_step()
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = ev[0].elapsed_time(ev[-1])
+    per_call = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(e2e_steps))
     e2e_ms = max_over_ranks(e2e_ms, dev)
     h2d = sum(pin[t].numel() * 2 for t in "qkv")
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
@@ -593,10 +598,13 @@ def run_fas(args, w):
         "e2e": {"value": job_tflops(world, flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / e2e_steps,
+                "ms_per_call_min_median_max": [per_call[0], per_call[len(per_call) // 2], per_call[-1]],
                 # Copy bandwidth between these pinned buffers and the device,
-                # taken outside the timed region: the host side of the box
-                # sets how far the copies can hide behind the kernels.
+                # taken just before and just after the timed region: the
+                # host side of the box (its memory is shared with other
+                # work) sets how far the copies can hide behind the kernels.
                 "pinned_h2d_gbs": copy_gbs[0], "pinned_d2h_gbs": copy_gbs[1],
+                "pinned_h2d_gbs_before": copy_before[0], "pinned_d2h_gbs_before": copy_before[1],
                 "overlap_check": overlap},
         "gpu_launches": timed_launches,
         "clocks": clocks,

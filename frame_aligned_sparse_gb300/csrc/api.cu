@@ -44,6 +44,11 @@ struct State {
   float* stat = nullptr;
   uint8_t* elig = nullptr;
   unsigned int* sync = nullptr;
+  // A second set of the prepass's per-launch scratch (centred and query
+  // partials, counters), for fas_forward_host's second compute stream.
+  float* kmax_part2 = nullptr;
+  float* gmax_part2 = nullptr;
+  unsigned int* sync2 = nullptr;
   unsigned int* err = nullptr;
   unsigned int* flags = nullptr;  // kFlagBoundRange (attention); cleared by fas_status
   const void* pre_q = nullptr;
@@ -61,7 +66,8 @@ struct State {
   int gwork_hg = -1;                 // heads_per_group argument the regrouped list was built for
   std::vector<int> grp_h0;           // first head of each group (plus H)
   std::vector<int> gwork_off;        // first item of each group (plus the end)
-  cudaStream_t st_h2d = nullptr, st_comp = nullptr, st_d2h = nullptr;
+  cudaStream_t st_h2d = nullptr, st_d2h = nullptr;
+  cudaStream_t st_comp[2] = {nullptr, nullptr};  // head groups alternate between the two
   std::vector<cudaEvent_t> ev_in, ev_done;
   cudaEvent_t ev_entry = nullptr, ev_exit = nullptr;
   bool exit_recorded = false;
@@ -120,9 +126,9 @@ void release() {
     int cur = -1;
     cudaGetDevice(&cur);
     if (s.device >= 0 && cur != s.device) cudaSetDevice(s.device);
-    for (cudaStream_t st : {s.st_h2d, s.st_comp, s.st_d2h})
+    for (cudaStream_t st : {s.st_h2d, s.st_comp[0], s.st_comp[1], s.st_d2h})
       if (st) cudaStreamSynchronize(st);
-    for (cudaStream_t st : {s.st_h2d, s.st_comp, s.st_d2h})
+    for (cudaStream_t st : {s.st_h2d, s.st_comp[0], s.st_comp[1], s.st_d2h})
       if (st) cudaStreamDestroy(st);
     for (auto* evs : {&s.ev_in, &s.ev_done})
       for (cudaEvent_t e : *evs) cudaEventDestroy(e);
@@ -179,6 +185,9 @@ int allocate(const HostPlan& p) {
       {H * 4, (void**)&s.stat},
       {H, (void**)&s.elig},
       {fas::prepass_sync_words(p.H, p.Nf) * 4, (void**)&s.sync},
+      {PI * 4, (void**)&s.kmax_part2},
+      {PI * 4, (void**)&s.gmax_part2},
+      {fas::prepass_sync_words(p.H, p.Nf) * 4, (void**)&s.sync2},
       {sizeof(unsigned int), (void**)&s.err},
       {sizeof(unsigned int), (void**)&s.flags},
   };
@@ -221,10 +230,13 @@ int64_t head_stride() {
   return g_state.layout == FAS_LAYOUT_NHD ? (int64_t)p.d : p.N * (int64_t)p.d;
 }
 
-// Prepass arguments for heads [h0, h0 + nh) of q and k (every per-head
-// statistics buffer is head-major, so it is offset by h0; the per-item
-// partial results are the launch's own scratch, from the start).
-fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
+// Prepass arguments for heads [h0, h0 + nh) of q and k.  Every per-head
+// statistics buffer is head-major, so it is offset by h0, and so are the
+// key partials (sized for every head); the centred and query partials and
+// the counters are a launch's own scratch, one of two sets: launches that
+// may run at once (fas_forward_host's two compute streams) use different
+// sets.
+fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh, int set = 0) {
   const HostPlan& p = g_state.plan;
   State& s = g_state;
   const size_t H0 = (size_t)h0, Nf = p.Nf, D = p.d, N = (size_t)p.N;
@@ -238,9 +250,9 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   a.R0 = p.R0;
   a.r = p.r;
   a.key_sums = nullptr;
-  a.ksum_part = s.ksum_part;  // launches run one at a time (one stream)
-  a.kmax_part = s.kmax_part;
-  a.gmax_part = s.gmax_part;
+  a.ksum_part = s.ksum_part + H0 * Nf * (size_t)s.chunks_k * D;
+  a.kmax_part = set ? s.kmax_part2 : s.kmax_part;
+  a.gmax_part = set ? s.gmax_part2 : s.gmax_part;
   a.mu = s.mu + H0 * D;
   a.fsum = s.fsum + H0 * Nf * D;
   a.frame_max = s.frame_max + H0 * Nf;
@@ -250,7 +262,7 @@ fas::PrepassArgs prepass_args(const void* q, const void* k, int h0, int nh) {
   a.row_bound = s.row_bound + H0 * N;
   a.stat = s.stat + H0;
   a.elig = s.elig + H0;
-  a.sync = s.sync;  // one launch at a time: the calls that launch the prepass serialise on one stream
+  a.sync = set ? s.sync2 : s.sync;
   a.err = s.err;
   a.N = p.N;
   a.T = p.T;
@@ -328,7 +340,8 @@ cudaError_t copy_heads(uint16_t* dst, const uint16_t* src, int nh, cudaMemcpyKin
 
 // fas_forward_host resources: device copies of the inputs and outputs, the
 // work list regrouped by head group (heaviest items first inside a group),
-// three streams and the per-group events.  Built on first use per plan.
+// four streams (copy in, two for compute, copy out) and the per-group
+// events.  Built on first use per plan.
 int ensure_host_pipeline(int hg) {
   State& s = g_state;
   const HostPlan& p = s.plan;
@@ -348,7 +361,7 @@ int ensure_host_pipeline(int hg) {
     if (encode_qkv(s.dq, s.dk, s.dv, &s.io_tq, &s.io_tk, &s.io_tv) != FAS_OK) return FAS_ERR_CUDA;
   }
   if (!s.st_h2d) {
-    for (cudaStream_t* st : {&s.st_h2d, &s.st_comp, &s.st_d2h})
+    for (cudaStream_t* st : {&s.st_h2d, &s.st_comp[0], &s.st_comp[1], &s.st_d2h})
       if (cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) != cudaSuccess) return FAS_ERR_CUDA;
     for (cudaEvent_t* e : {&s.ev_entry, &s.ev_exit})
       if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
@@ -641,7 +654,7 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
   // Start after the caller's earlier work, and after the previous call of
   // this function has finished with the library's device copies.
   if (cudaEventRecord(s.ev_entry, caller) != cudaSuccess) return FAS_ERR_CUDA;
-  for (cudaStream_t st : {s.st_h2d, s.st_comp, s.st_d2h}) {
+  for (cudaStream_t st : {s.st_h2d, s.st_comp[0], s.st_comp[1], s.st_d2h}) {
     if (cudaStreamWaitEvent(st, s.ev_entry, 0) != cudaSuccess) return FAS_ERR_CUDA;
     if (s.exit_recorded && cudaStreamWaitEvent(st, s.ev_exit, 0) != cudaSuccess) return FAS_ERR_CUDA;
   }
@@ -666,17 +679,21 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
     return cudaEventRecord(s.ev_in[g], s.st_h2d) == cudaSuccess;
   };
   auto compute = [&](int g) -> bool {
-    // Prepass and attention for the group's heads.
+    // Prepass and attention for the group's heads, on the group's compute
+    // stream with its set of prepass scratch.  Groups alternate between the
+    // two, so the next group's launches take the SMs the current group's
+    // last CTAs leave idle; they share nothing but the error words.
     const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
-    if (cudaStreamWaitEvent(s.st_comp, s.ev_in[g], 0) != cudaSuccess) return false;
-    const int np = fas::launch_prepass(prepass_args(s.dq, s.dk, h0, nh), s.st_comp);
+    cudaStream_t st = s.st_comp[g & 1];
+    if (cudaStreamWaitEvent(st, s.ev_in[g], 0) != cudaSuccess) return false;
+    const int np = fas::launch_prepass(prepass_args(s.dq, s.dk, h0, nh, g & 1), st);
     if (np < 0) return false;
     launches += np;
     const int i0 = s.gwork_off[g], ni = s.gwork_off[g + 1] - i0;
-    if (launch_fwd(s.io_tq, s.io_tk, s.io_tv, s.gwork + i0, ni, s.dout, s.dlse, mode, s.st_comp) != cudaSuccess)
+    if (launch_fwd(s.io_tq, s.io_tk, s.io_tv, s.gwork + i0, ni, s.dout, s.dlse, mode, st) != cudaSuccess)
       return false;
     ++launches;
-    return cudaEventRecord(s.ev_done[g], s.st_comp) == cudaSuccess;
+    return cudaEventRecord(s.ev_done[g], st) == cudaSuccess;
   };
   auto copy_out = [&](int g) -> bool {
     // The group's rows of out and lse.

@@ -200,9 +200,11 @@ int fas_forward(const void* q, const void* k, const void* v, void* out, float* l
  * current layout ([H, N, d], or [N, H, d] after fas_set_layout); lse: host
  * fp32 [H, N]; results as for fas_prepass followed by fas_forward
  * (bit-identical outputs).  The heads are independent, so the
- * call splits them into groups and pipelines the groups on three
+ * call splits them into groups and pipelines the groups on four
  * library-owned streams: while group g is computed (prepass and attention),
- * group g+1 is copied in and group g-1 copied out.  heads_per_group > 0
+ * group g+1 is copied in and group g-1 copied out; consecutive groups
+ * compute on two alternating streams, so a group's launches can start on
+ * the SMs the previous group's last CTAs leave idle.  heads_per_group > 0
  * gives groups of that many heads; 0 gives the default schedule, which
  * ramps up (1, 2, then 4 heads per group) so that the first copy-in, which
  * nothing hides, is short, and ends with a one-head group so that the last
