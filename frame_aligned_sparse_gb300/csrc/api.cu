@@ -68,7 +68,7 @@ struct State {
   std::vector<int> gwork_off;        // first item of each group (plus the end)
   cudaStream_t st_h2d = nullptr, st_d2h = nullptr;
   cudaStream_t st_comp[2] = {nullptr, nullptr};  // head groups alternate between the two
-  std::vector<cudaEvent_t> ev_in, ev_done;
+  std::vector<cudaEvent_t> ev_qk, ev_in, ev_done;  // per group: q and k in, v in, computed
   cudaEvent_t ev_entry = nullptr, ev_exit = nullptr;
   bool exit_recorded = false;
   // fas_forward_ablation: both passes' work lists and fp32 intermediates.
@@ -130,7 +130,7 @@ void release() {
       if (st) cudaStreamSynchronize(st);
     for (cudaStream_t st : {s.st_h2d, s.st_comp[0], s.st_comp[1], s.st_d2h})
       if (st) cudaStreamDestroy(st);
-    for (auto* evs : {&s.ev_in, &s.ev_done})
+    for (auto* evs : {&s.ev_qk, &s.ev_in, &s.ev_done})
       for (cudaEvent_t e : *evs) cudaEventDestroy(e);
     for (cudaEvent_t e : {s.ev_entry, s.ev_exit})
       if (e) cudaEventDestroy(e);
@@ -369,7 +369,7 @@ int ensure_host_pipeline(int hg) {
   if (s.gwork_hg != hg) s.grp_h0 = head_groups(p.H, hg);
   const int groups = (int)s.grp_h0.size() - 1;
   while ((int)s.ev_in.size() < groups) {
-    for (auto* evs : {&s.ev_in, &s.ev_done}) {
+    for (auto* evs : {&s.ev_qk, &s.ev_in, &s.ev_done}) {
       cudaEvent_t e = nullptr;
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return FAS_ERR_CUDA;
       evs->push_back(e);
@@ -670,12 +670,17 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
     // slice of every token's row, copied as a 2D block.
     const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
     const size_t off = (size_t)h0 * (size_t)head_stride();
-    const void* src[3] = {q, k, v};
-    uint16_t* dst[3] = {s.dq, s.dk, s.dv};
-    for (int t = 0; t < 3; ++t)
+    // k and q first: the group's prepass needs only those, so it starts
+    // while v is still coming in (this hides part of the first group's
+    // copy, which nothing else hides).
+    const void* src[3] = {k, q, v};
+    uint16_t* dst[3] = {s.dk, s.dq, s.dv};
+    for (int t = 0; t < 3; ++t) {
       if (copy_heads(dst[t] + off, static_cast<const uint16_t*>(src[t]) + off, nh, cudaMemcpyHostToDevice,
                      s.st_h2d) != cudaSuccess)
         return false;
+      if (t == 1 && cudaEventRecord(s.ev_qk[g], s.st_h2d) != cudaSuccess) return false;
+    }
     return cudaEventRecord(s.ev_in[g], s.st_h2d) == cudaSuccess;
   };
   auto compute = [&](int g) -> bool {
@@ -685,10 +690,11 @@ int fas_forward_host(const void* q, const void* k, const void* v, void* out, flo
     // last CTAs leave idle; they share nothing but the error words.
     const int h0 = s.grp_h0[g], nh = s.grp_h0[g + 1] - h0;
     cudaStream_t st = s.st_comp[g & 1];
-    if (cudaStreamWaitEvent(st, s.ev_in[g], 0) != cudaSuccess) return false;
+    if (cudaStreamWaitEvent(st, s.ev_qk[g], 0) != cudaSuccess) return false;
     const int np = fas::launch_prepass(prepass_args(s.dq, s.dk, h0, nh, g & 1), st);
     if (np < 0) return false;
     launches += np;
+    if (cudaStreamWaitEvent(st, s.ev_in[g], 0) != cudaSuccess) return false;
     const int i0 = s.gwork_off[g], ni = s.gwork_off[g + 1] - i0;
     if (launch_fwd(s.io_tq, s.io_tk, s.io_tv, s.gwork + i0, ni, s.dout, s.dlse, mode, st) != cudaSuccess)
       return false;

@@ -291,6 +291,15 @@ def test_edge_geometries(spec):
     for mode in ("auto", "online"):
         _, out, lse = c.run(mode, block_k=bk)
         c.check(out, lse, f"{name}/{mode}")
+    # The prepass fed the 16-token key sums (key items cut at 16-row
+    # boundaries of frames as short as 16 tokens), then the attention on
+    # its bounds.
+    elig = fas.fas_prepass_with_key_sums(c.q, c.k, key_sums_of(c.x["k"]), want_elig=True)
+    got = fas.fas_prepass_readback(row_bound=True)
+    check_key_sums_statistics(c, got, elig)
+    out, lse = fas.fas_forward(c.q, c.k, c.v, mode="auto")
+    assert fas.fas_status() == fas.FAS_OK
+    c.check(out, lse, f"{name}/auto/key sums")
 
 
 def test_outputs_are_bit_reproducible():
