@@ -121,8 +121,10 @@ def job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> floa
 
 
 def prepass_algorithmic_bytes(H: int, N: int, d: int) -> int:
-    """The prepass reads K and Q once (bf16) and writes one fp32 bound per
-    row; the per-head statistics are a few hundred KB more and not counted."""
+    """Algorithmic bytes of the prepass: one read of K and of Q (bf16) and
+    one fp32 bound per row written; the per-head statistics are a few
+    hundred KB more and not counted.  (The kernel fed k alone reads K a
+    second time for the centred norms: traffic, not algorithmic bytes.)"""
     return 2 * H * N * d * 2 + H * N * 4
 
 
