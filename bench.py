@@ -456,15 +456,19 @@ def run_fas(args, w):
     # results are on the host): the spread of the per-call times shows
     # whether the copies kept pace throughout.
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    e2e_sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()
+    e2e_sampler.start()
+    time.sleep(0.2)
     ev[0].record(stream)
     for i in range(e2e_steps):
         e2e_step()
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
+    e2e_clocks = e2e_sampler.stop()
     e2e_ms = ev[0].elapsed_time(ev[-1])
-    per_call = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(e2e_steps))
+    per_call = [ev[i].elapsed_time(ev[i + 1]) for i in range(e2e_steps)]
     e2e_ms = max_over_ranks(e2e_ms, dev)
     h2d = sum(pin[t].numel() * 2 for t in "qkv")
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
@@ -600,7 +604,8 @@ def run_fas(args, w):
         "e2e": {"value": job_tflops(world, flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / e2e_steps,
-                "ms_per_call_min_median_max": [per_call[0], per_call[len(per_call) // 2], per_call[-1]],
+                "ms_per_call": [round(t, 3) for t in per_call],
+                "clocks": e2e_clocks,
                 # Copy bandwidth between these pinned buffers and the device,
                 # taken just before and just after the timed region: the
                 # host side of the box (its memory is shared with other
