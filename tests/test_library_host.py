@@ -183,6 +183,25 @@ def test_noalloc_wrapper_rejects_a_geometry_that_does_not_match_q():
         fas.fas_prepass_noalloc(q, q, 64, 8, 1, 1, rb, stat, elig)
 
 
+def test_key_sums_calls_check_their_arguments_before_any_device_work():
+    """The prologue's key-sums output and the prepass that takes it refuse
+    bad arguments before touching memory (the pointers below are never
+    dereferenced)."""
+    lib = fas.load()
+    lib.fas_free()
+    p = 256
+    assert lib.fas_prepass_with_key_sums(p, p, None, None, None) == fas.FAS_ERR_ARG
+    assert lib.fas_prepass_with_key_sums(p, p, p, None, None) == fas.FAS_ERR_STATE  # no plan
+    four = (p, p, p, p)
+    assert lib.fas_prologue_with_key_sums(*four, 120, 128, 2, 64, 1e-6, p, p, p, 0, 1, 1, p,
+                                          None) == fas.FAS_ERR_ARG  # tokens not a multiple of 16
+    assert lib.fas_prologue_with_key_sums(*four, 128, 128, 2, 64, 1e-6, p, p, p, 0, 1, 1, p + 8,
+                                          None) == fas.FAS_ERR_ALIGN
+    assert fas.key_sums_shape(24, 79200, 128) == (24, 4950, 128)
+    with pytest.raises(ValueError):
+        fas.key_sums_shape(2, 120, 64)
+
+
 def test_block_size_choice_matches_frame_spans():
     # Largest multiple of 16 dividing T within the on-chip budget (<= 160).
     for T, want in ((48, 48), (880, 80), (3600, 144), (8160, 160), (16, 16), (4096, 128), (192, 96), (352, 32), (320, 160), (400, 80)):
